@@ -1,0 +1,20 @@
+"""Oracle package: a plain fp64 CPU restatement of the DSpark context-KV write.
+
+TEST INFRASTRUCTURE ONLY.  Imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; never by the library, which has no
+CPU fallback.  It shares no code with the CUDA path.
+
+Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
+  stacked_ctx_kv_params  refusal cases + stacked == per-layer (exact, brute force)
+  kv_proj_only           brute-force triple loop (exact), identity / one-hot closed forms
+  apply_k_norm           constant-vector closed form, mean-square and scale invariants
+  apply_k_rope           position-0 identity, pair-norm, complex-rotation equality,
+                         quarter-turn table, hand-worked golden example
+  written_tokens         hand-worked window golden example, -1 / commit edge cases
+  write_target_hidden_kv composition of the above + bias closed form
+"""
+from .ctx_kv import (  # noqa: F401
+    LayerDesc, Stacked, WriteArgError, WriteResult, apply_k_norm, apply_k_rope,
+    kv_proj_only, layer_descs, per_layer_reference, project_stacked, run_workload,
+    stacked_ctx_kv_params, widen, write_target_hidden_kv, written_tokens,
+)

@@ -1,0 +1,252 @@
+"""Seeded synthetic inputs for the DSpark context-KV write.
+
+This module only draws random numbers and lays them out in the storage formats
+that both sides consume (raw bf16/fp16 bit patterns, int64 indices, an fp32
+cos/sin table).  It holds none of the write's arithmetic: no projection, no
+norm, no rotation, no scatter rule.  The oracle and the CUDA path each read the
+same host buffers produced here.
+
+Shapes follow the draft-model context-KV write described on the sglang PR
+#31986 summary page ("write_target_hidden_kv" snippet: ctx_hidden [T, H],
+per-layer qkv_proj.weight [q_size + 2*kv_size, H], k_norm weight [head_dim])
+and the sglang PR #31847 summary page ("_build_fused_kv_write_bundle" and
+"fused_kv_norm_rope_write" snippets: pools [slots, num_kv_heads, head_dim],
+cos/sin cache rows [cos | sin] of width head_dim, flattened [bs, W] verify
+windows with commit_lens).
+
+Five named workloads:
+
+* ``tiny``       T=32,    H=256,  L=2, NH=2, D=64,  bf16, no bias, 1-D locs
+* ``decode512``  T=512,   H=4096, L=5, NH=8, D=128, bf16, 64 requests x 8 window
+* ``prefill32k`` T=32768, H=4096, L=5, NH=8, D=128, bf16, 8 requests x 4096, 1% -1
+* ``fp16bias``   T=4096,  H=5120, L=8, NH=8, D=128, fp16 + bias, 256 x 16 window
+* ``k3gqa``      T=2048,  H=7168, L=5, NH=8, D=64,  bf16, 256 x 8 window
+
+``make_workload(name, seed=None, **overrides)`` builds one; overrides change
+T-independent sizes for sweeps (``tokens`` keeps the decode shapes but changes
+the request count).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional
+
+import numpy as np
+
+BF16 = "bf16"
+FP16 = "fp16"
+
+# Bit pattern written into every pool slot before a write; any slot that the
+# write must not touch keeps it.  0xDEAD is a finite bf16 / a finite fp16.
+POOL_SENTINEL = 0xDEAD
+# Quiet-NaN bit pattern for the Q rows of the synthetic qkv weights, so that a
+# path which reads outside the KV slice produces NaN outputs.
+QNAN_BITS = {BF16: 0x7FC1, FP16: 0x7E01}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (round to nearest, ties to even); finite inputs."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+def f32_to_fp16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to IEEE fp16 (numpy's conversion rounds to nearest even)."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    return f32_to_bf16_bits(x) if dtype == BF16 else f32_to_fp16_bits(x)
+
+
+@dataclasses.dataclass
+class Layer:
+    """One draft layer's attention parameters as a model would hold them."""
+    qkv_weight: np.ndarray            # uint16 bits [q_size + 2*kv_size, H]
+    qkv_bias: Optional[np.ndarray]    # uint16 bits [q_size + 2*kv_size] or None
+    k_norm_weight: np.ndarray         # uint16 bits [head_dim] (model dtype)
+    eps: float
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    seed: int
+    dtype: str                        # "bf16" | "fp16"
+    T: int
+    H: int
+    L: int
+    NH: int
+    D: int
+    q_size: int
+    layers: List[Layer]
+    ctx_hidden: np.ndarray            # uint16 bits [T, H]
+    positions: np.ndarray             # int64 [T]
+    cos_sin: np.ndarray               # float32 [max_pos, D], row = [cos | sin]
+    cache_loc: np.ndarray             # int64 [T] (flattened [bs, W] in window mode)
+    commit_lens: Optional[np.ndarray]  # int32 [bs] or None
+    loc_row_width: int                # W in window mode, 0 otherwise
+    pool_slots: int
+    rope_base: float
+
+    @property
+    def KV(self) -> int:
+        return self.NH * self.D
+
+    @property
+    def N(self) -> int:
+        return self.L * 2 * self.KV
+
+    @property
+    def max_pos(self) -> int:
+        return int(self.cos_sin.shape[0])
+
+    @property
+    def eps(self) -> float:
+        return self.layers[0].eps
+
+    @property
+    def has_bias(self) -> bool:
+        return self.layers[0].qkv_bias is not None
+
+
+def rope_cos_sin_table(max_pos: int, head_dim: int, base: float) -> np.ndarray:
+    """Precomputed neox cos/sin cache, fp32, one row per position.
+
+    Row p holds cos(p * base**(-2i/D)) for i < D/2, then the matching sines
+    (the layout the table-lookup kernels on the sglang PR #31847 page index as
+    ``pos * D + i`` and ``pos * D + D/2 + i``).  Angles are formed in fp64 and
+    the cos/sin values rounded once to fp32.  The table is an input of the
+    write: it is built here, outside both implementations.
+    """
+    half = head_dim // 2
+    inv_freq = base ** (-np.arange(half, dtype=np.float64) * 2.0 / head_dim)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def _layers(rng, dtype, L, H, q_size, KV, D, eps, bias_std):
+    layers = []
+    rows = q_size + 2 * KV
+    for _ in range(L):
+        w = np.empty((rows, H), dtype=np.uint16)
+        w[:q_size] = QNAN_BITS[dtype]
+        w[q_size:] = to_bits(rng.standard_normal((2 * KV, H), dtype=np.float32)
+                             * np.float32(H ** -0.5), dtype)
+        b = None
+        if bias_std is not None:
+            b = np.empty((rows,), dtype=np.uint16)
+            b[:q_size] = QNAN_BITS[dtype]
+            b[q_size:] = to_bits(rng.standard_normal(2 * KV, dtype=np.float32)
+                                 * np.float32(bias_std), dtype)
+        knw = to_bits(1.0 + 0.1 * rng.standard_normal(D, dtype=np.float32), dtype)
+        layers.append(Layer(qkv_weight=w, qkv_bias=b, k_norm_weight=knw, eps=eps))
+    return layers
+
+
+def _hidden(rng, T, H, dtype):
+    return to_bits(rng.standard_normal((T, H), dtype=np.float32), dtype)
+
+
+def _distinct_slots(rng, n, slots):
+    return rng.permutation(slots)[:n].astype(np.int64)
+
+
+def _window_commit(rng, bs, lo, hi):
+    return rng.integers(lo, hi + 1, size=bs).astype(np.int32)
+
+
+def make_workload(name: str, seed: Optional[int] = None, **kw) -> Workload:
+    """Build one named synthetic workload (bit-identical for a given seed)."""
+    seeds = {"tiny": 0, "decode512": 1, "prefill32k": 2, "fp16bias": 3, "k3gqa": 4}
+    if name not in seeds:
+        raise KeyError(f"unknown workload {name!r}; have {sorted(seeds)}")
+    seed = seeds[name] if seed is None else seed
+    rng = np.random.default_rng(seed)
+
+    if name == "tiny":
+        dtype, H, L, NH, D = BF16, kw.get("H", 256), kw.get("L", 2), 2, 64
+        T = kw.get("tokens", 32)
+        KV, q_size, eps, base, max_pos = NH * D, 2 * NH * D, 1e-6, 1e6, 4096
+        slots = kw.get("pool_slots", max(256, T))
+        layers = _layers(rng, dtype, L, H, q_size, KV, D, eps, None)
+        x = _hidden(rng, T, H, dtype)
+        pos = rng.integers(0, 4000, size=T).astype(np.int64)
+        loc = _distinct_slots(rng, T, slots)
+        commit, width = None, 0
+
+    elif name in ("decode512", "k3gqa"):
+        if name == "decode512":
+            dtype, H, L, NH, D = BF16, 4096, 5, 8, 128
+            q_size, slots, max_pos = 4 * NH * D, 65536, 65536
+        else:
+            dtype, H, L, NH, D = BF16, 7168, 5, 8, 64
+            q_size, slots, max_pos = 4 * NH * D, 262144, 131072
+        width = 8
+        T = kw.get("tokens", 512 if name == "decode512" else 2048)
+        if T % width:
+            raise ValueError("window-mode token count must be a multiple of 8")
+        bs = T // width
+        KV, eps, base = NH * D, 1e-6, 1e6
+        slots = kw.get("pool_slots", slots)
+        layers = _layers(rng, dtype, L, H, q_size, KV, D, eps, None)
+        x = _hidden(rng, T, H, dtype)
+        if name == "decode512":
+            ctx = rng.integers(1024, 32768 + 1, size=bs).astype(np.int64)
+            pos = (ctx[:, None] + np.arange(width, dtype=np.int64)[None, :]).reshape(-1)
+        else:
+            pos = rng.integers(0, 131071, size=T).astype(np.int64)
+        loc = _distinct_slots(rng, T, slots)
+        commit = _window_commit(rng, bs, 1, width)
+
+    elif name == "prefill32k":
+        dtype, H, L, NH, D = BF16, 4096, 5, 8, 128
+        req_len = kw.get("req_len", 4096)
+        nreq = kw.get("requests", 8)
+        T = nreq * req_len
+        KV, q_size, eps, base, max_pos = NH * D, 4 * NH * D, 1e-6, 1e6, 4096
+        slots = kw.get("pool_slots", 40000 if T <= 40000 else T + T // 5)
+        layers = _layers(rng, dtype, L, H, q_size, KV, D, eps, None)
+        x = _hidden(rng, T, H, dtype)
+        pos = np.tile(np.arange(req_len, dtype=np.int64), nreq)
+        # non-overlapping contiguous slot ranges, random order, random gaps
+        spare = slots - T
+        cuts = np.sort(rng.integers(0, spare + 1, size=nreq))
+        order = rng.permutation(nreq)
+        bases = np.empty(nreq, dtype=np.int64)
+        for k, r in enumerate(order):
+            bases[r] = cuts[k] + k * req_len
+        loc = (bases[:, None] + np.arange(req_len, dtype=np.int64)[None, :]).reshape(-1)
+        loc[rng.random(T) < 0.01] = -1
+        commit, width = None, 0
+
+    else:  # fp16bias
+        dtype, H, L, NH, D = FP16, 5120, 8, 8, 128
+        width = 16
+        T = kw.get("tokens", 4096)
+        bs = T // width
+        KV, q_size, eps, base, max_pos = NH * D, 4 * NH * D, 1e-5, 1e6, 131072
+        slots = kw.get("pool_slots", 65536)
+        layers = _layers(rng, dtype, L, H, q_size, KV, D, eps, 0.02)
+        x = _hidden(rng, T, H, dtype)
+        start = rng.integers(0, 131056, size=bs).astype(np.int64)
+        pos = (start[:, None] + np.arange(width, dtype=np.int64)[None, :]).reshape(-1)
+        loc = _distinct_slots(rng, T, slots)
+        commit = _window_commit(rng, bs, 0, width)
+
+    return Workload(
+        name=name, seed=seed, dtype=dtype, T=T, H=H, L=L, NH=NH, D=D, q_size=q_size,
+        layers=layers, ctx_hidden=x, positions=pos.astype(np.int64),
+        cos_sin=rope_cos_sin_table(max_pos, D, base), cache_loc=loc.astype(np.int64),
+        commit_lens=commit, loc_row_width=width, pool_slots=slots, rope_base=base)
+
+
+WORKLOADS = ("tiny", "decode512", "prefill32k", "fp16bias", "k3gqa")
+
+
+def describe(w: Workload) -> Dict[str, object]:
+    return {"workload": w.name, "tokens": w.T, "hidden": w.H, "layers": w.L,
+            "kv_heads": w.NH, "head_dim": w.D, "dtype": w.dtype, "bias": w.has_bias,
+            "window": w.loc_row_width, "pool_slots": w.pool_slots, "max_pos": w.max_pos,
+            "seed": w.seed}
