@@ -1,0 +1,386 @@
+"""Benchmark of the DSpark context-KV write on GB300.
+
+One step = one dspark_write_ctx_kv call over the whole workload: the stacked
+K|V projection of every token, K RMSNorm, table RoPE and the scatter into
+every layer's pool.  Default workload: the Qwen3-8B-shaped draft decode
+(T=512 = 64 requests x 8-token windows, H=4096, 5 layers, 8 kv heads x 128,
+bf16, commit_lens truncation, 65536-slot pools).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints ONE JSON line (rank 0).  `value` is device time: CUDA events on the
+launching stream around each step, inputs resident in HBM, the L2 flushed
+(256 MiB write) between steps outside the events.  `e2e` is the same metric
+through the public API with pinned host inputs: host->device copies of the
+step's inputs, the write, and a device->host read of the status word, timed
+on the host.  `--impl reference` times the CPU oracle instead (the reference
+arm of this build: there is no other implementation to run).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ctx-KV tokens/s (stacked proj+norm+RoPE+pool write); % of roofline"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def work_per_step(w, written_rows):
+    """Algorithmic FLOPs and bytes of one step (DESIGN: roofline accounting)."""
+    s = 2
+    flops = 2.0 * w.T * w.N * w.H
+    bytes_ = w.N * w.H * s + w.T * w.H * s + written_rows * w.N * s
+    return flops, bytes_
+
+
+# ----------------------------------------------------------------- clocks (NVML, read-only)
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x1: "gpu_idle", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index=0, period_s=0.002):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.period = period_s
+        self.ok = False
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+                return
+            m = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        while not self.stop:
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(r)) == 0:
+                self.reasons |= r.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        self.stop = False
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self.stop = True
+        if self.ok:
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"],
+                    "samples": 0}
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- oracle timing
+
+def oracle_rate(w, sample_tokens=None, min_seconds=10.0, max_reps=8):
+    """Tokens/s of the CPU oracle on `w` (all tokens, or a fixed sample)."""
+    import numpy as np
+    import oracle
+    reps, t0 = 0, time.perf_counter()
+    n = w.T if sample_tokens is None else len(sample_tokens)
+    while True:
+        oracle.run_workload(w, sample=sample_tokens)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return n * reps / el, reps, el
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(tokens_local: float, seconds_local: float, group=None):
+    """Whole-job throughput: tokens of all ranks over the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return tokens_local / seconds_local, seconds_local, tokens_local
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([seconds_local], dtype=torch.float64, device=dev)
+    n = torch.tensor([tokens_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM, group=group)
+    return n.item() / t.item(), t.item(), n.item()
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- arms
+
+def run_reference(args, w):
+    """The oracle as the reference arm: each step is the oracle on a fixed
+    sample of the workload's tokens."""
+    import numpy as np
+    import oracle
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    written = oracle.written_tokens(w.cache_loc, w.commit_lens,
+                                    w.loc_row_width if w.commit_lens is not None else None)
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(written, size=min(args.ref_sample, written.size), replace=False))
+    for _ in range(args.warmup):
+        oracle.run_workload(w, sample=sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_workload(w, sample=sample)
+    el = time.perf_counter() - t0
+    val = len(sample) * args.steps / el
+    desc = (f"{len(sample)} written tokens of {w.name} per step (all layers, K and V), "
+            f"numpy float64 oracle")
+    return {
+        "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference", "config": config_of(w, flush=False),
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_of(w, flush=True):
+    import synthetic
+    c = synthetic.describe(w)
+    c["parallelism"] = "replicas (one independent write per GPU, no collective)"
+    c["l2"] = "flushed between steps (256 MiB write)" if flush else "n/a (CPU)"
+    return c
+
+
+def run_gpu(args, w):
+    import numpy as np
+    import torch
+    import draft_model_kv_gb300 as dk
+    import oracle
+    from draft_model_kv_gb300 import build as _build
+    from synthetic.device import stage
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    _build.build()
+    st = stage(w, device=f"cuda:{local}")
+    bundle = dk.dspark_pack_ctx_kv(st["layers"], w.H)
+    for lay in st["layers"]:          # the bundle holds its own copy of the K|V rows
+        lay.qkv_weight = None
+    torch.cuda.empty_cache()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
+    written = oracle.written_tokens(w.cache_loc, w.commit_lens,
+                                    w.loc_row_width if w.commit_lens is not None else None)
+
+    def step(x=None, pos=None, loc=None, cl=None):
+        dk.dspark_write_ctx_kv(bundle, st["ctx_hidden"] if x is None else x,
+                               st["positions"] if pos is None else pos, st["cos_sin"],
+                               st["cache_loc"] if loc is None else loc, st["k_pools"], st["v_pools"],
+                               commit_lens=st["commit_lens"] if cl is None else cl,
+                               loc_row_width=st["loc_row_width"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    dk.dspark_clear_device_status(bundle)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: K steps, one kernel each, L2 flushed between
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dev_s = sum(per_step_ms) / 1e3
+    flags = dk.dspark_get_device_status(bundle)
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} during the timed region")
+    value, t_max, n_all = aggregate(w.T * args.steps, dev_s)
+
+    # ---- end to end through the public API with pinned host inputs
+    host_x = st["ctx_hidden"].cpu().pin_memory()
+    host_pos = st["positions"].cpu().pin_memory()
+    host_loc = st["cache_loc"].cpu().pin_memory()
+    host_cl = None if st["commit_lens"] is None else st["commit_lens"].cpu().pin_memory()
+    dx = torch.empty_like(st["ctx_hidden"])
+    dpos = torch.empty_like(st["positions"])
+    dloc = torch.empty_like(st["cache_loc"])
+    dcl = None if host_cl is None else torch.empty_like(st["commit_lens"])
+    status_host = ctypes.c_uint32()
+    h2d = host_x.numel() * 2 + host_pos.numel() * 8 + host_loc.numel() * 8 + \
+        (0 if host_cl is None else host_cl.numel() * 4)
+    e2e_total = 0.0
+    e2e_steps = max(1, min(args.steps, 200))
+    for i in range(e2e_steps + 3):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dx.copy_(host_x, non_blocking=True)
+        dpos.copy_(host_pos, non_blocking=True)
+        dloc.copy_(host_loc, non_blocking=True)
+        if dcl is not None:
+            dcl.copy_(host_cl, non_blocking=True)
+        step(dx, dpos, dloc, dcl)
+        flags = dk.dspark_get_device_status(bundle, stream)   # d2h of the status word + sync
+        t1 = time.perf_counter()
+        if i >= 3:
+            e2e_total += t1 - t0
+        if flags:
+            raise RuntimeError(f"device status flags {flags:#x} in the e2e loop")
+    e2e_value, _, _ = aggregate(w.T * e2e_steps, e2e_total)
+
+    if rank != 0:
+        return None
+    flops, bytes_ = work_per_step(w, len(written))
+    pk = peaks()
+    mean_ms = statistics.mean(per_step_ms)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = bytes_ / (pk["hbm_gbs"] * 1e9)
+    achieved_tf = flops / (mean_ms * 1e-3) / 1e12
+    achieved_gb = bytes_ / (mean_ms * 1e-3) / 1e9
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    traffic = ncu_traffic(w.name)
+    roof_tc = {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16_tflops"],
+               "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16_tflops"], "traffic": traffic,
+               "peak_source": pk["source"] + " (burst: the kernel is timed alone)"}
+    roof_hbm = {"bound": "hbm", "achieved": achieved_gb, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gb / pk["hbm_gbs"], "traffic": traffic,
+                "peak_source": pk["source"]}
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "fp16", "data": "synthetic",
+        "config": config_of(w),
+        "roofline": roof_tc if bound == "tensor" else roof_hbm,
+        "roofline_other": roof_hbm if bound == "tensor" else roof_tc,
+        "roofline_time_frac": max(t_tc, t_hbm) / (mean_ms * 1e-3),
+        "ms_per_step_median": statistics.median(per_step_ms),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 4, "steps": e2e_steps,
+                "timing": "host wall clock per step: h2d inputs + write + status d2h + sync"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        rate, reps, el = oracle_rate(w, min_seconds=args.cpu_seconds)
+        out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                               "sample": f"whole {w.name} workload ({w.T} tokens) x {reps} runs, "
+                                         f"{el:.1f} s, numpy float64 (BLAS threads = cores)"}
+    bundle.free()
+    return out
+
+
+NCU_TRAFFIC = {
+    # per-launch DRAM bytes (read + write) of the fused kernel from one ncu
+    # capture; null until a capture of the current kernel exists
+}
+
+
+def ncu_traffic(name):
+    return NCU_TRAFFIC.get(name)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode512")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--ref-sample", type=int, default=64)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    import synthetic
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        w = synthetic.make_workload(args.workload)
+        out = run_reference(args, w)
+        print(json.dumps(out))
+        return 0
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    w = synthetic.make_workload(args.workload)
+    out = run_gpu(args, w)
+    if out is not None:
+        print(json.dumps(out))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,180 @@
+"""DSpark draft-model context-KV write on one GB300 (sm_103a).
+
+Python binding of the C ABI declared in include/dspark_ctx_kv.h, with the
+same entry-point names.  It only marshals arguments: torch tensors supply
+device pointers, strides and the current CUDA stream; every step of the write
+runs in the library's CUDA kernels.  Importing works without a GPU (the
+host-only eligibility check can run); GPU calls raise when the library is not
+built or no sm_103 device is present.  There is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+from . import _abi
+from ._abi import (DSparkError, FLAG_LOC_RANGE, FLAG_POS_RANGE, FLAG_TIMEOUT,  # noqa: F401
+                   LayerDesc, load)
+
+__all__ = [
+    "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
+    "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
+    "dspark_status_string", "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
+]
+
+
+def _dtype_code(t) -> int:
+    import torch
+    return {torch.bfloat16: _abi.DTYPE_BF16, torch.float16: _abi.DTYPE_FP16,
+            torch.float32: _abi.DTYPE_FP32}.get(t, _abi.DTYPE_OTHER)
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+@dataclass
+class Layer:
+    """One draft layer's attention parameters (device tensors)."""
+    qkv_weight: object                 # [q_size + 2*kv_size (or more), hidden]
+    k_norm_weight: object              # [head_dim]
+    eps: float
+    q_size: int
+    num_kv_heads: int
+    head_dim: int
+    qkv_bias: object = None            # [rows] or None
+
+    def desc(self) -> LayerDesc:
+        w = self.qkv_weight
+        if w.dim() != 2 or w.stride(1) != 1:
+            raise ValueError("qkv_weight must be a 2-D tensor with unit column stride")
+        return LayerDesc(
+            qkv_weight=w.data_ptr(), qkv_rows=w.shape[0], qkv_row_stride=w.stride(0),
+            qkv_bias=None if self.qkv_bias is None else self.qkv_bias.data_ptr(),
+            k_norm_weight=self.k_norm_weight.data_ptr(), weight_dtype=_dtype_code(w.dtype),
+            k_norm_dtype=_dtype_code(self.k_norm_weight.dtype), q_size=self.q_size,
+            num_kv_heads=self.num_kv_heads, head_dim=self.head_dim, eps=self.eps)
+
+
+def _desc_array(layers: Sequence) -> ctypes.Array:
+    descs = [l if isinstance(l, LayerDesc) else l.desc() for l in layers]
+    arr = (LayerDesc * max(1, len(descs)))()
+    for i, d in enumerate(descs):
+        arr[i] = d
+    return arr
+
+
+def dspark_check_ctx_kv_layers(layers: Sequence, hidden: int) -> int:
+    """Host-only eligibility check; returns the status code (0 = stackable)."""
+    arr = _desc_array(layers)
+    return load().dspark_check_ctx_kv_layers(arr, len(layers), hidden)
+
+
+def dspark_status_string(code: int) -> str:
+    return load().dspark_status_string(code).decode()
+
+
+class Bundle:
+    """Owner of a packed dspark_bundle_t (freed on garbage collection)."""
+
+    def __init__(self, handle: int):
+        self.handle = ctypes.c_void_p(handle)
+        info = _abi.BundleInfo()
+        _abi.check(load().dspark_bundle_get_info(self.handle, ctypes.byref(info)),
+                   "dspark_bundle_get_info")
+        self.num_layers = info.num_layers
+        self.hidden = info.hidden
+        self.num_kv_heads = info.num_kv_heads
+        self.head_dim = info.head_dim
+        self.dtype_code = info.dtype
+        self.has_bias = bool(info.has_bias)
+        self.device = info.device
+        self.eps = info.eps
+        self.stacked_rows = info.stacked_rows
+
+    def free(self) -> None:
+        if self.handle is not None and self.handle.value:
+            load().dspark_free_bundle(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def dspark_pack_ctx_kv(layers: Sequence, hidden: int, stream=None) -> Bundle:
+    """Stack every layer's K|V projection slice into a library-owned bundle."""
+    arr = _desc_array(layers)
+    out = ctypes.c_void_p()
+    _abi.check(load().dspark_pack_ctx_kv(arr, len(layers), hidden, _stream_handle(stream),
+                                         ctypes.byref(out)), "dspark_pack_ctx_kv")
+    return Bundle(out.value)
+
+
+def _ptr_array(tensors):
+    arr = (ctypes.c_void_p * len(tensors))()
+    for i, t in enumerate(tensors):
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def dspark_write_ctx_kv(bundle: Bundle, ctx_hidden, positions, cos_sin, cache_loc, k_pools,
+                        v_pools, commit_lens=None, loc_row_width: Optional[int] = None,
+                        stream=None) -> None:
+    """Write K (normed, roped) and V of every token into every layer's pool.
+
+    ctx_hidden [T, hidden] (bundle dtype, unit column stride); positions and
+    cache_loc int64 [T]; cos_sin fp32 [max_pos, head_dim]; commit_lens int32
+    [bs] with loc_row_width W (bs * W == T) or neither; k_pools / v_pools: one
+    [slots, num_kv_heads, head_dim] tensor per layer with head/dim strides
+    (head_dim, 1).  Asynchronous on `stream` (default: torch's current stream).
+    """
+    import torch
+    T = ctx_hidden.shape[0]
+    if ctx_hidden.dim() != 2 or (T > 0 and ctx_hidden.stride(1) != 1):
+        raise ValueError("ctx_hidden must be [T, hidden] with unit column stride")
+    for name, t, dt in (("positions", positions, torch.int64), ("cache_loc", cache_loc, torch.int64),
+                        ("cos_sin", cos_sin, torch.float32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous {dt} tensor")
+    if commit_lens is not None and (commit_lens.dtype != torch.int32 or not commit_lens.is_contiguous()):
+        raise TypeError("commit_lens must be a contiguous int32 tensor")
+    if len(k_pools) != bundle.num_layers or len(v_pools) != bundle.num_layers:
+        raise ValueError("one K and one V pool per layer")
+    slots = k_pools[0].shape[0]
+    for p in list(k_pools) + list(v_pools):
+        if p.dtype != k_pools[0].dtype:
+            raise TypeError("all pools must share one dtype")
+        if (p.dim() != 3 or p.shape[0] != slots or p.shape[1] != bundle.num_kv_heads
+                or p.shape[2] != bundle.head_dim or p.stride(1) != bundle.head_dim or p.stride(2) != 1):
+            raise ValueError("pools must be [slots, num_kv_heads, head_dim] with strides (*, head_dim, 1)")
+    width = 0 if loc_row_width is None else int(loc_row_width)
+    nwin = 0 if commit_lens is None else commit_lens.numel()
+    L = bundle.num_layers
+    kstr = (ctypes.c_int64 * L)(*[p.stride(0) for p in k_pools])
+    vstr = (ctypes.c_int64 * L)(*[p.stride(0) for p in v_pools])
+    code = load().dspark_write_ctx_kv(
+        bundle.handle, ctx_hidden.data_ptr(), T, ctx_hidden.stride(0) if T > 0 else ctx_hidden.shape[1],
+        _dtype_code(ctx_hidden.dtype), positions.data_ptr(), cos_sin.data_ptr(), cos_sin.shape[0],
+        cache_loc.data_ptr(), None if commit_lens is None else commit_lens.data_ptr(), width, nwin,
+        _ptr_array(k_pools), _ptr_array(v_pools), kstr, vstr, _dtype_code(k_pools[0].dtype), slots,
+        _stream_handle(stream))
+    _abi.check(code, "dspark_write_ctx_kv")
+
+
+def dspark_get_device_status(bundle: Bundle, stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    _abi.check(load().dspark_get_device_status(bundle.handle, _stream_handle(stream),
+                                               ctypes.byref(flags)), "dspark_get_device_status")
+    return flags.value
+
+
+def dspark_clear_device_status(bundle: Bundle, stream=None) -> None:
+    _abi.check(load().dspark_clear_device_status(bundle.handle, _stream_handle(stream)),
+               "dspark_clear_device_status")

@@ -1,0 +1,199 @@
+/*
+ * dspark_ctx_kv.h -- C ABI of the DSpark draft-model context-KV write on one
+ * GB300 GPU (sm_103a).
+ *
+ * The write (sglang PR #31986 summary page, "write_target_hidden_kv" snippet;
+ * sglang PR #31847 summary page, "fused_kv_norm_rope_write" snippet):
+ *
+ *   for every draft layer l, token t, kv head h, d in [0, D):
+ *     yK = ctx_hidden[t] . W_qkv,l[q_size + h*D + d]        (+ bias)
+ *     yV = ctx_hidden[t] . W_qkv,l[q_size + KV + h*D + d]   (+ bias)
+ *     n  = yK / sqrt(mean_d(yK^2) + eps) * k_norm_l[d]        (fp32 weights)
+ *     K  = neox rotation of n by the cos/sin row positions[t] of the table
+ *     if cache_loc[t] >= 0 (and, in window mode, t's column < commit_lens[row]):
+ *       K_pool_l[cache_loc[t]][h][:] = K,  V_pool_l[cache_loc[t]][h][:] = yV
+ *
+ * computed as ONE dense product of ctx_hidden with the row-stacked K|V slices
+ * of every layer (the inputs are shared, so stacking is exact: PR #31986 page,
+ * "Motivation") followed by a fused norm / rotation / scatter epilogue.
+ *
+ * Conventions
+ *  - Pointers are DEVICE pointers unless marked (host).  Element strides are
+ *    counted in elements, not bytes.
+ *  - Every call returns a dspark_status (0 = success).  Argument errors are
+ *    detected on the host before any GPU work is enqueued; nothing is
+ *    allocated or written when a call is refused.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Writes
+ *    are asynchronous and stream-ordered; caller-owned buffers must stay
+ *    alive until the stream work completes.
+ *  - The library has no CPU fallback: without a usable sm_103 GPU the GPU
+ *    calls return DSPARK_E_CUDA / DSPARK_E_DEVICE.
+ */
+#ifndef DSPARK_CTX_KV_H
+#define DSPARK_CTX_KV_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+#define DSPARK_DTYPE_BF16 1
+#define DSPARK_DTYPE_FP16 2
+#define DSPARK_DTYPE_FP32 3   /* accepted for k_norm weights only */
+/* Any other weight_dtype code (e.g. a quantized format) marks the layer's
+ * qkv weight as non-sliceable and the pack is refused. */
+
+typedef enum dspark_status {
+  DSPARK_OK = 0,
+  DSPARK_E_INVALID_ARG = 1,       /* NULL pointer, negative size, ... */
+  DSPARK_E_NO_LAYERS = 2,         /* num_layers == 0 */
+  DSPARK_E_NOT_SLICEABLE = 3,     /* a qkv weight is not plain bf16/fp16 (quantized) */
+  DSPARK_E_EPS_MISMATCH = 4,      /* layers disagree on the k_norm epsilon */
+  DSPARK_E_DTYPE_MISMATCH = 5,    /* layers / activations / pools of different dtype */
+  DSPARK_E_SHAPE_MISMATCH = 6,    /* layers disagree on q_size, num_kv_heads or head_dim,
+                                     or a weight has fewer rows than q_size + 2*kv_size */
+  DSPARK_E_HEAD_DIM = 7,          /* head_dim not 64 or 128 */
+  DSPARK_E_BIAS_MISMATCH = 8,     /* bias on some layers only */
+  DSPARK_E_COMMIT_ARGS = 9,       /* commit_lens and loc_row_width not given together */
+  DSPARK_E_NUMEL = 10,            /* num_windows * loc_row_width != num_tokens */
+  DSPARK_E_ALIGNMENT = 11,        /* a buffer or stride breaks the 16-byte rules below */
+  DSPARK_E_POOL_LAYOUT = 12,      /* pool row stride < num_kv_heads * head_dim */
+  DSPARK_E_TOO_MANY_LAYERS = 13,  /* num_layers > DSPARK_MAX_LAYERS */
+  DSPARK_E_DEVICE = 14,           /* no sm_103 device, or not the bundle's device */
+  DSPARK_E_CUDA = 15,             /* a CUDA runtime call failed */
+  DSPARK_E_DEVICE_FAULT = 16      /* a device-side check fired (see status flags) */
+} dspark_status;
+
+#define DSPARK_MAX_LAYERS 32
+
+/* Bits of the device status word (dspark_get_device_status).  The write skips
+ * the offending token and sets the bit; other tokens are still written. */
+#define DSPARK_FLAG_POS_RANGE 0x1u   /* positions[t] < 0 or >= max_pos */
+#define DSPARK_FLAG_LOC_RANGE 0x2u   /* cache_loc[t] >= pool_slots */
+#define DSPARK_FLAG_TIMEOUT   0x4u   /* an in-kernel wait exceeded its bound; output incomplete */
+
+/* One draft layer's attention parameters, as the model holds them
+ * (PR #31986 page, _stacked_ctx_kv_params; PR #31847 page,
+ * _build_fused_kv_write_bundle).  (host) struct, device buffers. */
+typedef struct dspark_layer_desc {
+  const void* qkv_weight;     /* [qkv_rows, hidden] row-major, out-by-in (F.linear);
+                                 rows [q_size, q_size+kv_size) are K, the next kv_size are V */
+  int64_t qkv_rows;           /* rows in qkv_weight, >= q_size + 2*kv_size */
+  int64_t qkv_row_stride;     /* elements between rows, >= hidden */
+  const void* qkv_bias;       /* NULL or [qkv_rows] in weight_dtype */
+  const void* k_norm_weight;  /* [head_dim] in k_norm_dtype; converted to fp32 */
+  int32_t weight_dtype;       /* DSPARK_DTYPE_BF16 | DSPARK_DTYPE_FP16, else non-sliceable */
+  int32_t k_norm_dtype;       /* BF16 | FP16 | FP32 */
+  int32_t q_size;             /* Q rows that precede the K rows */
+  int32_t num_kv_heads;       /* NH; kv_size = NH * head_dim */
+  int32_t head_dim;           /* D: 64 or 128 */
+  float eps;                  /* k_norm variance epsilon */
+} dspark_layer_desc;
+
+typedef struct dspark_bundle* dspark_bundle_t;
+
+/* Read-only view of a packed bundle. (host) */
+typedef struct dspark_bundle_info {
+  int32_t num_layers, hidden, num_kv_heads, head_dim, dtype, has_bias, device;
+  float eps;
+  int64_t stacked_rows;       /* N = num_layers * 2 * num_kv_heads * head_dim */
+} dspark_bundle_info;
+
+/*
+ * dspark_check_ctx_kv_layers -- host-only eligibility check of a set of layers.
+ * Touches no GPU and reads no device memory.  Returns DSPARK_OK or the first
+ * refusal, in this order: E_INVALID_ARG, E_NO_LAYERS, E_TOO_MANY_LAYERS, then
+ * per layer E_NOT_SLICEABLE, E_EPS_MISMATCH, E_DTYPE_MISMATCH,
+ * E_SHAPE_MISMATCH, E_HEAD_DIM, and finally E_BIAS_MISMATCH.  The refusals
+ * follow PR #31986's _stacked_ctx_kv_params (quantized weight, eps mismatch,
+ * partial bias -> no stacked bundle) and PR #31847's bundle builder (same
+ * head_dim and kv_size on every layer).
+ */
+DSPARK_API int dspark_check_ctx_kv_layers(const dspark_layer_desc* layers /* (host) [num_layers] */,
+                               int32_t num_layers, int32_t hidden);
+
+/*
+ * dspark_pack_ctx_kv -- build the immutable stacked bundle.
+ * Copies rows [q_size, q_size + 2*kv_size) of every layer's qkv weight into one
+ * bundle-owned [N, hidden] matrix (rows l0:K, l0:V, l1:K, ...), the matching
+ * bias rows (when every layer has a bias), and the k_norm weights as fp32
+ * [L, head_dim]; records eps.  Runs the check above first and allocates
+ * nothing on refusal.  The bundle is owned by the library: free it with
+ * dspark_free_bundle.  It is bound to the device current at the call.  The
+ * copies run on `stream` and the call synchronises that stream before it
+ * returns, so the bundle is ready for use on any stream.  The bundle keeps a
+ * snapshot: if the model's weights change, pack again (PR #31986 page, Risks:
+ * the cached stack assumes frozen weights).
+ */
+DSPARK_API int dspark_pack_ctx_kv(const dspark_layer_desc* layers /* (host) [num_layers] */,
+                       int32_t num_layers, int32_t hidden, void* stream,
+                       dspark_bundle_t* out /* (host) */);
+
+/*
+ * dspark_write_ctx_kv -- project, normalise, rotate and scatter K/V of
+ * num_tokens tokens into every layer's pool (PR #31847 page,
+ * fused_kv_norm_rope_write: loc < 0 is skipped; with commit_lens the locs are
+ * a flattened [num_windows, loc_row_width] verify window and only the first
+ * commit_lens[b] columns of row b are written).
+ *
+ *  ctx_hidden      [num_tokens, hidden] in the bundle dtype, row stride
+ *                  hidden_row_stride (>= hidden); base and row pitch 16-byte aligned
+ *  positions       [num_tokens] int64, each in [0, max_pos)
+ *  cos_sin         [max_pos, head_dim] fp32, row p = [cos(p*f_0..f_{D/2-1}) | sin(...)],
+ *                  16-byte aligned.  Neox pairing, full rotary dimension.
+ *  cache_loc       [num_tokens] int64 pool slots; < 0 = skip
+ *  commit_lens     NULL, or [num_windows] int32 (<= 0 writes nothing, > width acts as width)
+ *  loc_row_width   0 when commit_lens is NULL, else the window width W > 0
+ *  num_windows     0 when commit_lens is NULL, else bs with bs * W == num_tokens
+ *  k_pools/v_pools (host) arrays of num_layers device pointers, each pool
+ *                  [pool_slots, num_kv_heads, head_dim] with row stride
+ *                  k_row_strides[l] / v_row_strides[l] (host arrays, elements,
+ *                  >= num_kv_heads*head_dim, multiple of 8) and head/dim
+ *                  strides head_dim / 1; 16-byte aligned bases
+ *  pool_dtype      must equal the bundle dtype
+ * Written non-negative locs must be distinct.  A position outside the table or
+ * a loc >= pool_slots is a caller error: that token is skipped and a device
+ * status flag is set.  num_tokens == 0 returns DSPARK_OK at once.
+ * Enqueues one kernel on `stream`; no host synchronisation.
+ */
+DSPARK_API int dspark_write_ctx_kv(dspark_bundle_t bundle,
+                        const void* ctx_hidden, int64_t num_tokens,
+                        int64_t hidden_row_stride, int32_t hidden_dtype,
+                        const int64_t* positions,
+                        const float* cos_sin, int64_t max_pos,
+                        const int64_t* cache_loc,
+                        const int32_t* commit_lens, int64_t loc_row_width,
+                        int64_t num_windows,
+                        void* const* k_pools, void* const* v_pools,
+                        const int64_t* k_row_strides, const int64_t* v_row_strides,
+                        int32_t pool_dtype, int64_t pool_slots,
+                        void* stream);
+
+/* Copy the bundle's device status word (DSPARK_FLAG_* bits, OR-ed over all
+ * writes since the last clear) to *flags, ordered after prior work on
+ * `stream`; synchronises `stream`. */
+DSPARK_API int dspark_get_device_status(dspark_bundle_t bundle, void* stream, uint32_t* flags /* (host) */);
+
+/* Reset the device status word to 0 (stream-ordered, asynchronous). */
+DSPARK_API int dspark_clear_device_status(dspark_bundle_t bundle, void* stream);
+
+DSPARK_API int dspark_bundle_get_info(dspark_bundle_t bundle, dspark_bundle_info* info /* (host) */);
+
+/* Release the bundle's device memory (synchronises the device first). NULL is a no-op. */
+DSPARK_API void dspark_free_bundle(dspark_bundle_t bundle);
+
+/* Static English text for a status code. */
+DSPARK_API const char* dspark_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_CTX_KV_H */

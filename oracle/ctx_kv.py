@@ -198,9 +198,11 @@ def per_layer_reference(ctx_hidden: np.ndarray, layers: Sequence[LayerDesc],
         dt = lay.weight_dtype
         x = widen(ctx_hidden, dt, acc)
         kv_size = lay.num_kv_heads * lay.head_dim
-        w = widen(lay.qkv_weight, dt, acc)
-        b = None if lay.qkv_bias is None else widen(lay.qkv_bias, dt, acc)
-        k, v = kv_proj_only(x, w, b, lay.q_size, kv_size)
+        # only the K|V rows are ever read: widen those (Q rows stay untouched)
+        rows = slice(lay.q_size, lay.q_size + 2 * kv_size)
+        w = widen(lay.qkv_weight[rows], dt, acc)
+        b = None if lay.qkv_bias is None else widen(lay.qkv_bias[rows], dt, acc)
+        k, v = kv_proj_only(x, w, b, 0, kv_size)
         kn = widen(lay.k_norm_weight, lay.k_norm_dtype or dt, np.float32).astype(acc)
         k = apply_k_norm(k, kn, lay.eps, lay.num_kv_heads, lay.head_dim)
         k = apply_k_rope(positions, k, cos_sin, lay.num_kv_heads, lay.head_dim)
