@@ -86,6 +86,9 @@ struct dspark_bundle {
   void* bias;           // [N] in dtype or null
   float* knorm;         // [L, D] fp32
   uint32_t* status;     // device status word
+  float* workspace;     // partial tiles of the stream-K split (workspace_bytes(sms))
+  int32_t* counters;    // [sms] arrival counters, zero between launches
+  int sms;              // SM count of the bundle's device
   float eps;
   CUtensorMap tmap_w;
 };
@@ -179,17 +182,25 @@ int dspark_pack_ctx_kv(const dspark_layer_desc* layers, int32_t num_layers, int3
   b->N = static_cast<int64_t>(num_layers) * 2 * b->KV;
   b->w_pitch = (hidden + 7) / 8 * 8;   // 16-byte row pitch for TMA
   b->eps = f.eps;
+  b->sms = device_sm_count(device);
+  if (b->sms <= 0) {
+    delete b;
+    return DSPARK_E_CUDA;
+  }
 
   const size_t es = 2;
   bool ok = cudaMalloc(&b->w_all, static_cast<size_t>(b->N) * b->w_pitch * es) == cudaSuccess &&
             cudaMalloc(reinterpret_cast<void**>(&b->knorm), sizeof(float) * num_layers * b->D) ==
                 cudaSuccess &&
-            cudaMalloc(reinterpret_cast<void**>(&b->status), sizeof(uint32_t)) == cudaSuccess;
+            cudaMalloc(reinterpret_cast<void**>(&b->status), sizeof(uint32_t)) == cudaSuccess &&
+            cudaMalloc(reinterpret_cast<void**>(&b->workspace), workspace_bytes(b->sms)) == cudaSuccess &&
+            cudaMalloc(reinterpret_cast<void**>(&b->counters), sizeof(int32_t) * b->sms) == cudaSuccess;
   if (ok && f.qkv_bias != nullptr)
     ok = cudaMalloc(&b->bias, static_cast<size_t>(b->N) * es) == cudaSuccess;
   if (ok && b->w_pitch != hidden)
     ok = cudaMemsetAsync(b->w_all, 0, static_cast<size_t>(b->N) * b->w_pitch * es, stream) == cudaSuccess;
   if (ok) ok = cudaMemsetAsync(b->status, 0, sizeof(uint32_t), stream) == cudaSuccess;
+  if (ok) ok = cudaMemsetAsync(b->counters, 0, sizeof(int32_t) * b->sms, stream) == cudaSuccess;
   for (int l = 0; ok && l < num_layers; ++l) {
     const dspark_layer_desc& a = layers[l];
     const int64_t rows = 2 * b->KV;
@@ -268,6 +279,10 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
   p.num_kb = (b->H + kTileK - 1) / kTileK;
   p.num_tiles = p.num_m * p.num_n;
+  int grid = 0;
+  plan_schedule(p.num_tiles, p.num_kb, b->sms, &grid, &p.dp_tiles, &p.sk_units);
+  p.workspace = b->workspace;
+  p.counters = b->counters;
   p.positions = positions;
   p.cache_loc = cache_loc;
   p.commit_lens = commit_lens;
@@ -286,9 +301,6 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
     p.k_stride[l] = k_row_strides[l];
     p.v_stride[l] = v_row_strides[l];
   }
-  const int sms = device_sm_count(device);
-  if (sms <= 0) return DSPARK_E_CUDA;
-  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
   const cudaError_t e =
       launch_tiled(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w, p, grid, stream);
   return e == cudaSuccess ? DSPARK_OK : DSPARK_E_CUDA;
@@ -307,8 +319,10 @@ int dspark_get_device_status(dspark_bundle_t b, void* stream_, uint32_t* flags) 
 
 int dspark_clear_device_status(dspark_bundle_t b, void* stream_) {
   if (b == nullptr) return DSPARK_E_INVALID_ARG;
-  return cudaMemsetAsync(b->status, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream_)) ==
-                 cudaSuccess
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  // the arrival counters are reset too: a launch that timed out may leave them set
+  return cudaMemsetAsync(b->status, 0, sizeof(uint32_t), stream) == cudaSuccess &&
+                 cudaMemsetAsync(b->counters, 0, sizeof(int32_t) * b->sms, stream) == cudaSuccess
              ? DSPARK_OK
              : DSPARK_E_CUDA;
 }
@@ -337,6 +351,8 @@ void dspark_free_bundle(dspark_bundle_t b) {
   if (b->bias) cudaFree(b->bias);
   if (b->knorm) cudaFree(b->knorm);
   if (b->status) cudaFree(b->status);
+  if (b->workspace) cudaFree(b->workspace);
+  if (b->counters) cudaFree(b->counters);
   if (prev >= 0) cudaSetDevice(prev);
   delete b;
 }

@@ -68,6 +68,7 @@ struct SmemBarriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int last_arrival;   // set by the epilogue leader when this CTA finishes a cut tile
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk,
@@ -92,6 +93,55 @@ __device__ __forceinline__ void store32(void* dst, const uint32_t (&w)[16]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// Work of one CTA: first its whole tiles of the data-parallel waves, then its
+// contiguous range of the stream-K k-block space.
+struct WorkIter {
+  int dp_tile;
+  int64_t cur, end;
+};
+
+__device__ __forceinline__ WorkIter work_begin(const WriteParams& p) {
+  WorkIter it;
+  it.dp_tile = blockIdx.x;
+  it.cur = static_cast<int64_t>(blockIdx.x) * p.sk_units / gridDim.x;
+  it.end = static_cast<int64_t>(blockIdx.x + 1) * p.sk_units / gridDim.x;
+  return it;
+}
+
+__device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, int& tile, int& kb0,
+                                          int& kb1) {
+  if (it.dp_tile < p.dp_tiles) {
+    tile = it.dp_tile;
+    kb0 = 0;
+    kb1 = p.num_kb;
+    it.dp_tile += gridDim.x;
+    return true;
+  }
+  if (it.cur < it.end) {
+    const int64_t t = it.cur / p.num_kb;
+    kb0 = static_cast<int>(it.cur - t * p.num_kb);
+    const int64_t rem = it.end - it.cur;
+    kb1 = rem < static_cast<int64_t>(p.num_kb - kb0) ? kb0 + static_cast<int>(rem) : p.num_kb;
+    it.cur += kb1 - kb0;
+    tile = p.dp_tiles + static_cast<int>(t);
+    return true;
+  }
+  return false;
+}
+
+// CTA whose stream-K range holds k-block unit u.
+__device__ __forceinline__ int sk_owner(const WriteParams& p, int64_t u) {
+  return static_cast<int>(((u + 1) * gridDim.x - 1) / p.sk_units);
+}
+
+// Partial-tile slot of a CTA: [kTileN/4][kTileM] float4, so that the 32 rows
+// of a warp write one contiguous 512-byte run per 4 columns.
+constexpr int kSlotFloats = kTileM * kTileN;
+
+__device__ __forceinline__ float* ws_slot(const WriteParams& p, int cta, int slot) {
+  return p.workspace + (static_cast<size_t>(cta) * 2 + slot) * kSlotFloats;
 }
 
 template <typename E, int D, bool kBias>
@@ -147,10 +197,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       uint32_t phase = 0;
       uint32_t uses[kStages] = {};
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      WorkIter it = work_begin(p);
+      int tile, kb0, kb1;
+      while (ok && work_next(p, it, tile, kb0, kb1)) {
         int m_blk, n_blk;
         tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
@@ -189,7 +241,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      WorkIter it = work_begin(p);
+      int tile, kb0, kb1;
+      while (ok && work_next(p, it, tile, kb0, kb1)) {
         if (!mbar_wait(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort_flag,
                        p.wait_limit_ns)) {
           ok = false;
@@ -197,7 +251,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(&bars->full[stage]), phase, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
@@ -209,7 +263,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           for (int k = 0; k < kTileK / 16; ++k) {
             // advancing 16 elements along K = 32 bytes inside the swizzle atom
             umma_f16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
-                     idesc, (kb | k) != 0);
+                     idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           issued = true;
           umma_commit(smem_u32(&bars->empty[stage]));
@@ -241,9 +295,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     constexpr int kHalf = D / 2;
     const int quarter = warp % 4;                 // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;          // token row inside the tile
+    const int etid = threadIdx.x - 64;            // 0..127 among the epilogue threads
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    WorkIter it = work_begin(p);
+    int tile, kb0, kb1;
+    while (work_next(p, it, tile, kb0, kb1)) {
       int m_blk, n_blk;
       tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
       // the outcome must be warp-uniform: tcgen05.ld below is .sync.aligned
@@ -257,120 +314,182 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         break;
       }
       tc_fence_after();
-
-      // ---- per-token decision (same for every head of the tile)
       const int64_t t = static_cast<int64_t>(m_blk) * kTileM + row;
-      bool write = false;
-      int64_t loc = 0, pos = 0;
-      if (t < p.T) {
-        loc = p.cache_loc[t];
-        write = loc >= 0;
-        if (write && p.loc_row_width > 0) {
-          const int64_t b = t / p.loc_row_width;
-          if (t - b * p.loc_row_width >= static_cast<int64_t>(p.commit_lens[b])) write = false;
+      const uint32_t t_row = tmem_base + acc * kAccCols + (static_cast<uint32_t>(quarter * 32) << 16);
+
+      // ---- a tile cut between CTAs: publish this part; the last contributor
+      // to arrive adds the other parts into its accumulator and finishes it
+      bool finish = true;
+      if (kb0 != 0 || kb1 != p.num_kb) {
+        const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
+        const int c_first = sk_owner(p, u0);
+        const int c_last = sk_owner(p, u0 + p.num_kb - 1);
+        float4* mine = reinterpret_cast<float4*>(ws_slot(p, blockIdx.x, kb0 > 0 ? 0 : 1));
+#pragma unroll 1
+        for (int ch = 0; ch < kTileN / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(t_row + ch * 32, v);
+          if (t < p.T) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              __stcg(mine + (ch * 8 + j) * kTileM + row,
+                     make_float4(f32(v[4 * j]), f32(v[4 * j + 1]), f32(v[4 * j + 2]), f32(v[4 * j + 3])));
+          }
+          __syncwarp();
         }
-        if (write) {
-          pos = p.positions[t];
-          if (pos < 0 || pos >= p.max_pos) {
-            flag(p, DSPARK_FLAG_POS_RANGE);
-            write = false;
-          } else if (loc >= p.pool_slots) {
-            flag(p, DSPARK_FLAG_LOC_RANGE);
-            write = false;
+        __threadfence();
+        named_barrier(1, 128);
+        if (etid == 0) {
+          const int old = atomicAdd(p.counters + c_last, 1);
+          const int last = old == c_last - c_first;
+          if (last) p.counters[c_last] = 0;   // ready for the next launch
+          __threadfence();
+          *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
+        }
+        named_barrier(1, 128);
+        // (the flag is next written only after all 128 threads pass the first
+        // barrier of a later cut tile, i.e. after every thread has read it)
+        finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
+        if (finish) {
+          // accumulator += every other contributor's part
+#pragma unroll 1
+          for (int ch = 0; ch < kTileN / 32; ++ch) {
+            uint32_t v[32];
+            tmem_ld32(t_row + ch * 32, v);
+            if (t < p.T) {
+              for (int c = c_first; c <= c_last; ++c) {
+                if (c == static_cast<int>(blockIdx.x)) continue;
+                const float4* other =
+                    reinterpret_cast<const float4*>(ws_slot(p, c, c == c_first ? 1 : 0));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 q = __ldcg(other + (ch * 8 + j) * kTileM + row);
+                  v[4 * j] = __float_as_uint(f32(v[4 * j]) + q.x);
+                  v[4 * j + 1] = __float_as_uint(f32(v[4 * j + 1]) + q.y);
+                  v[4 * j + 2] = __float_as_uint(f32(v[4 * j + 2]) + q.z);
+                  v[4 * j + 3] = __float_as_uint(f32(v[4 * j + 3]) + q.w);
+                }
+              }
+            }
+            __syncwarp();
+            tmem_st32(t_row + ch * 32, v);
           }
         }
       }
-      const uint32_t t_row = tmem_base + acc * kAccCols + (static_cast<uint32_t>(quarter * 32) << 16);
+
+      if (finish) {
+        // ---- per-token decision (same for every head of the tile)
+        bool write = false;
+        int64_t loc = 0, pos = 0;
+        if (t < p.T) {
+          loc = p.cache_loc[t];
+          write = loc >= 0;
+          if (write && p.loc_row_width > 0) {
+            const int64_t b = t / p.loc_row_width;
+            if (t - b * p.loc_row_width >= static_cast<int64_t>(p.commit_lens[b])) write = false;
+          }
+          if (write) {
+            pos = p.positions[t];
+            if (pos < 0 || pos >= p.max_pos) {
+              flag(p, DSPARK_FLAG_POS_RANGE);
+              write = false;
+            } else if (loc >= p.pool_slots) {
+              flag(p, DSPARK_FLAG_LOC_RANGE);
+              write = false;
+            }
+          }
+        }
 
 #pragma unroll 1
-      for (int seg = 0; seg < kTileN / D; ++seg) {
-        const int c0 = n_blk * kTileN + seg * D;
-        if (c0 >= p.N) break;
-        const int layer = c0 / (2 * p.KV);
-        const int r = c0 - layer * 2 * p.KV;
-        const bool is_v = r >= p.KV;
-        const int head = (is_v ? r - p.KV : r) / D;
-        const uint32_t t_seg = t_row + seg * D;
-        if (is_v) {
-          E* dst = reinterpret_cast<E*>(p.v_pool[layer]) + loc * p.v_stride[layer] + head * D;
+        for (int seg = 0; seg < kTileN / D; ++seg) {
+          const int c0 = n_blk * kTileN + seg * D;
+          if (c0 >= p.N) break;
+          const int layer = c0 / (2 * p.KV);
+          const int r = c0 - layer * 2 * p.KV;
+          const bool is_v = r >= p.KV;
+          const int head = (is_v ? r - p.KV : r) / D;
+          const uint32_t t_seg = t_row + seg * D;
+          if (is_v) {
+            E* dst = reinterpret_cast<E*>(p.v_pool[layer]) + loc * p.v_stride[layer] + head * D;
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(t_seg + ch * 32, v);
-            if (write) {
-              uint32_t o[16];
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t v[32];
+              tmem_ld32(t_seg + ch * 32, v);
+              if (write) {
+                uint32_t o[16];
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                float a = f32(v[e]), b = f32(v[e + 1]);
-                if (kBias) {
-                  a += ElemOps<E>::load(p.bias, c0 + ch * 32 + e);
-                  b += ElemOps<E>::load(p.bias, c0 + ch * 32 + e + 1);
-                }
-                o[e / 2] = ElemOps<E>::pack(a, b);
-              }
-              store32(dst + ch * 32, o);
-            }
-            __syncwarp();
-          }
-        } else {
-          // RMSNorm: sum of squares over this thread's row of the head
-          float ss = 0.f;
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(t_seg + ch * 32, v);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float x = f32(v[e]);
-              if (kBias) x += ElemOps<E>::load(p.bias, c0 + ch * 32 + e);
-              ss = fmaf(x, x, ss);
-            }
-          }
-          const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
-          const float* w = p.knorm + static_cast<int64_t>(layer) * D;
-          const float* cs = p.cos_sin + pos * D;
-          E* dst = reinterpret_cast<E*>(p.k_pool[layer]) + loc * p.k_stride[layer] + head * D;
-#pragma unroll
-          for (int hc = 0; hc < kHalf / 32; ++hc) {
-            uint32_t a[32], b[32];
-            tmem_ld32(t_seg + hc * 32, a);
-            tmem_ld32(t_seg + kHalf + hc * 32, b);
-            if (write) {
-              uint32_t o1[16], o2[16];
-#pragma unroll
-              for (int e4 = 0; e4 < 32; e4 += 4) {
-                const int i = hc * 32 + e4;
-                const float4 w1 = *reinterpret_cast<const float4*>(w + i);
-                const float4 w2 = *reinterpret_cast<const float4*>(w + kHalf + i);
-                const float4 c4 = *reinterpret_cast<const float4*>(cs + i);
-                const float4 s4 = *reinterpret_cast<const float4*>(cs + kHalf + i);
-                const float wa[4] = {w1.x, w1.y, w1.z, w1.w};
-                const float wb[4] = {w2.x, w2.y, w2.z, w2.w};
-                const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-                const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
-                float r1[4], r2[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  float x1 = f32(a[e4 + j]);
-                  float x2 = f32(b[e4 + j]);
+                for (int e = 0; e < 32; e += 2) {
+                  float a = f32(v[e]), b = f32(v[e + 1]);
                   if (kBias) {
-                    x1 += ElemOps<E>::load(p.bias, c0 + i + j);
-                    x2 += ElemOps<E>::load(p.bias, c0 + kHalf + i + j);
+                    a += ElemOps<E>::load(p.bias, c0 + ch * 32 + e);
+                    b += ElemOps<E>::load(p.bias, c0 + ch * 32 + e + 1);
                   }
-                  x1 = x1 * inv * wa[j];
-                  x2 = x2 * inv * wb[j];
-                  r1[j] = x1 * cc[j] - x2 * sn[j];
-                  r2[j] = x2 * cc[j] + x1 * sn[j];
+                  o[e / 2] = ElemOps<E>::pack(a, b);
                 }
-                o1[e4 / 2] = ElemOps<E>::pack(r1[0], r1[1]);
-                o1[e4 / 2 + 1] = ElemOps<E>::pack(r1[2], r1[3]);
-                o2[e4 / 2] = ElemOps<E>::pack(r2[0], r2[1]);
-                o2[e4 / 2 + 1] = ElemOps<E>::pack(r2[2], r2[3]);
+                store32(dst + ch * 32, o);
               }
-              store32(dst + hc * 32, o1);
-              store32(dst + kHalf + hc * 32, o2);
+              __syncwarp();
             }
-            __syncwarp();
+          } else {
+            // RMSNorm: sum of squares over this thread's row of the head
+            float ss = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t v[32];
+              tmem_ld32(t_seg + ch * 32, v);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                float x = f32(v[e]);
+                if (kBias) x += ElemOps<E>::load(p.bias, c0 + ch * 32 + e);
+                ss = fmaf(x, x, ss);
+              }
+            }
+            const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
+            const float* w = p.knorm + static_cast<int64_t>(layer) * D;
+            const float* cs = p.cos_sin + pos * D;
+            E* dst = reinterpret_cast<E*>(p.k_pool[layer]) + loc * p.k_stride[layer] + head * D;
+#pragma unroll
+            for (int hc = 0; hc < kHalf / 32; ++hc) {
+              uint32_t a[32], b[32];
+              tmem_ld32(t_seg + hc * 32, a);
+              tmem_ld32(t_seg + kHalf + hc * 32, b);
+              if (write) {
+                uint32_t o1[16], o2[16];
+#pragma unroll
+                for (int e4 = 0; e4 < 32; e4 += 4) {
+                  const int i = hc * 32 + e4;
+                  const float4 w1 = *reinterpret_cast<const float4*>(w + i);
+                  const float4 w2 = *reinterpret_cast<const float4*>(w + kHalf + i);
+                  const float4 c4 = *reinterpret_cast<const float4*>(cs + i);
+                  const float4 s4 = *reinterpret_cast<const float4*>(cs + kHalf + i);
+                  const float wa[4] = {w1.x, w1.y, w1.z, w1.w};
+                  const float wb[4] = {w2.x, w2.y, w2.z, w2.w};
+                  const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+                  const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+                  float r1[4], r2[4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    float x1 = f32(a[e4 + j]);
+                    float x2 = f32(b[e4 + j]);
+                    if (kBias) {
+                      x1 += ElemOps<E>::load(p.bias, c0 + i + j);
+                      x2 += ElemOps<E>::load(p.bias, c0 + kHalf + i + j);
+                    }
+                    x1 = x1 * inv * wa[j];
+                    x2 = x2 * inv * wb[j];
+                    r1[j] = x1 * cc[j] - x2 * sn[j];
+                    r2[j] = x2 * cc[j] + x1 * sn[j];
+                  }
+                  o1[e4 / 2] = ElemOps<E>::pack(r1[0], r1[1]);
+                  o1[e4 / 2 + 1] = ElemOps<E>::pack(r1[2], r1[3]);
+                  o2[e4 / 2] = ElemOps<E>::pack(r2[0], r2[1]);
+                  o2[e4 / 2 + 1] = ElemOps<E>::pack(r2[2], r2[3]);
+                }
+                store32(dst + hc * 32, o1);
+                store32(dst + kHalf + hc * 32, o2);
+              }
+              __syncwarp();
+            }
           }
         }
       }

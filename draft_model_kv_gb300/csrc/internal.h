@@ -23,6 +23,14 @@ struct WriteParams {
   const void* bias;             // [N] or null
   float eps;
   uint32_t* status;             // device status word (DSPARK_FLAG_*)
+  // work split: the first dp_tiles tiles go whole to CTAs in waves of
+  // gridDim.x; the remaining tiles' k-blocks (sk_units of them) are cut into
+  // gridDim.x equal contiguous ranges ("stream-K"); a tile cut between CTAs is
+  // finished by whichever contributor arrives last (no CTA waits for another)
+  int32_t dp_tiles;
+  int64_t sk_units;
+  float* workspace;             // [gridDim.x][2][kTileN/4][kTileM][4] fp32 partial tiles
+  int32_t* counters;            // [gridDim.x] arrivals per cut tile, reset by the last one
   uint64_t wait_limit_ns;       // bound on any single in-kernel wait
   void* k_pool[DSPARK_MAX_LAYERS];
   void* v_pool[DSPARK_MAX_LAYERS];
@@ -38,7 +46,31 @@ constexpr int kStages = 4;
 constexpr int kTiledThreads = 192;
 constexpr int kGroupM = 8;     // m-blocks per raster group (L2 reuse of weight tiles)
 
+constexpr int kMinUnitsPerCta = 8;   // k-blocks: keeps small problems from over-splitting
+
 size_t tiled_smem_bytes();
+
+// Bytes of partial-tile workspace and arrival counters for a grid of `ctas`.
+inline size_t workspace_bytes(int ctas) {
+  return static_cast<size_t>(ctas) * 2 * kTileM * kTileN * sizeof(float);
+}
+
+// Grid size and data-parallel / stream-K split for a problem of `tiles`
+// output tiles with `num_kb` k-blocks each on `sms` SMs.
+inline void plan_schedule(int tiles, int num_kb, int sms, int* grid, int* dp_tiles,
+                          int64_t* sk_units) {
+  const int waves = tiles / sms;
+  *dp_tiles = waves >= 2 ? (waves - 1) * sms : 0;
+  *sk_units = static_cast<int64_t>(tiles - *dp_tiles) * num_kb;
+  if (*dp_tiles > 0) {
+    *grid = sms;
+  } else {
+    int64_t g = *sk_units / kMinUnitsPerCta;
+    if (g > sms) g = sms;
+    if (g < 1) g = 1;
+    *grid = static_cast<int>(g);
+  }
+}
 
 // Launch the tiled kernel for the bundle dtype (1 = bf16, 2 = fp16).  Returns
 // the CUDA error of the launch.
