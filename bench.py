@@ -327,7 +327,7 @@ def run_gpu(args, w):
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        rate, reps, el = oracle_rate(w, min_seconds=args.cpu_seconds)
+        rate, reps, el = oracle_rate(w, min_seconds=args.cpu_seconds, max_reps=1000)
         out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                                "sample": f"whole {w.name} workload ({w.T} tokens) x {reps} runs, "
                                          f"{el:.1f} s, numpy float64 (BLAS threads = cores)"}
@@ -345,12 +345,20 @@ def ncu_traffic(name):
     return NCU_TRAFFIC.get(name)
 
 
+def make(args):
+    import synthetic
+    kw = {} if args.tokens is None else {"tokens": args.tokens}
+    return synthetic.make_workload(args.workload, **kw)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="decode512")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="token count override (supplementary sweeps; keeps the workload's other sizes)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -363,7 +371,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        w = synthetic.make_workload(args.workload)
+        w = make(args)
         out = run_reference(args, w)
         print(json.dumps(out))
         return 0
@@ -372,7 +380,7 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-    w = synthetic.make_workload(args.workload)
+    w = make(args)
     out = run_gpu(args, w)
     if out is not None:
         print(json.dumps(out))

@@ -20,7 +20,7 @@ from ._abi import (DSparkError, FLAG_LOC_RANGE, FLAG_POS_RANGE, FLAG_TIMEOUT,  #
 __all__ = [
     "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
-    "dspark_status_string", "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
+    "dspark_status_string", "dspark_set_trace_buffer", "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
 
@@ -178,3 +178,13 @@ def dspark_get_device_status(bundle: Bundle, stream=None) -> int:
 def dspark_clear_device_status(bundle: Bundle, stream=None) -> None:
     _abi.check(load().dspark_clear_device_status(bundle.handle, _stream_handle(stream)),
                "dspark_clear_device_status")
+
+
+def dspark_set_trace_buffer(bundle: Bundle, buf) -> None:
+    """Record per-CTA timelines of later writes into `buf` (a uint64-sized
+    CUDA tensor of at least SMs x 64 words), or stop recording (None)."""
+    if buf is None:
+        code = load().dspark_set_trace_buffer(bundle.handle, None, 0)
+    else:
+        code = load().dspark_set_trace_buffer(bundle.handle, buf.data_ptr(), buf.numel())
+    _abi.check(code, "dspark_set_trace_buffer")

@@ -32,7 +32,7 @@ CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = (
     "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv", "dspark_write_ctx_kv",
     "dspark_get_device_status", "dspark_clear_device_status", "dspark_bundle_get_info",
-    "dspark_free_bundle", "dspark_status_string",
+    "dspark_free_bundle", "dspark_status_string", "dspark_set_trace_buffer",
 )
 
 
@@ -92,6 +92,8 @@ def load() -> ctypes.CDLL:
     lib.dspark_bundle_get_info.restype = ctypes.c_int
     lib.dspark_free_bundle.argtypes = [vp]
     lib.dspark_free_bundle.restype = None
+    lib.dspark_set_trace_buffer.argtypes = [vp, vp, i64]
+    lib.dspark_set_trace_buffer.restype = ctypes.c_int
     lib.dspark_status_string.argtypes = [ctypes.c_int]
     lib.dspark_status_string.restype = ctypes.c_char_p
     _lib = lib

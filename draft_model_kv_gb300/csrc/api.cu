@@ -89,6 +89,7 @@ struct dspark_bundle {
   float* workspace;     // partial tiles of the stream-K split (workspace_bytes(sms))
   int32_t* counters;    // [sms] arrival counters, zero between launches
   int sms;              // SM count of the bundle's device
+  uint64_t* trace;      // optional timeline buffer (dspark_set_trace_buffer)
   float eps;
   CUtensorMap tmap_w;
 };
@@ -282,6 +283,7 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   int grid = 0;
   plan_schedule(p.num_tiles, p.num_kb, b->sms, &grid, &p.dp_tiles, &p.sk_units);
   p.workspace = b->workspace;
+  p.trace = b->trace;
   p.counters = b->counters;
   p.positions = positions;
   p.cache_loc = cache_loc;
@@ -325,6 +327,13 @@ int dspark_clear_device_status(dspark_bundle_t b, void* stream_) {
                  cudaMemsetAsync(b->counters, 0, sizeof(int32_t) * b->sms, stream) == cudaSuccess
              ? DSPARK_OK
              : DSPARK_E_CUDA;
+}
+
+int dspark_set_trace_buffer(dspark_bundle_t b, uint64_t* buf, int64_t words) {
+  if (b == nullptr) return DSPARK_E_INVALID_ARG;
+  if (buf != nullptr && words < static_cast<int64_t>(b->sms) * kTraceWords) return DSPARK_E_INVALID_ARG;
+  b->trace = buf;
+  return DSPARK_OK;
 }
 
 int dspark_bundle_get_info(dspark_bundle_t b, dspark_bundle_info* info) {

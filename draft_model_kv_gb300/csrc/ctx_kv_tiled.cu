@@ -187,6 +187,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+  uint64_t* trace = p.trace != nullptr ? p.trace + static_cast<size_t>(blockIdx.x) * kTraceWords : nullptr;
+  if (trace != nullptr && threadIdx.x == 0) trace[0] = global_timer_ns();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -298,6 +300,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const int etid = threadIdx.x - 64;            // 0..127 among the epilogue threads
     int acc = 0;
     uint32_t acc_phase = 0;
+    int item = 0;
     WorkIter it = work_begin(p);
     int tile, kb0, kb1;
     while (work_next(p, it, tile, kb0, kb1)) {
@@ -306,6 +309,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // the outcome must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort_flag,
                                  p.wait_limit_ns);
+      uint64_t* tr = (trace != nullptr && etid == 0 && item < kTraceItems) ? trace + 3 + 4 * item : nullptr;
+      if (tr != nullptr) {
+        tr[0] = static_cast<uint64_t>(tile);
+        tr[1] = (static_cast<uint64_t>(kb0) << 16) | static_cast<uint64_t>(kb1);
+        tr[2] = global_timer_ns();
+      }
+      ++item;
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
           *abort_flag = 1;
@@ -343,6 +353,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           const int old = atomicAdd(p.counters + c_last, 1);
           const int last = old == c_last - c_first;
           if (last) p.counters[c_last] = 0;   // ready for the next launch
+          if (tr != nullptr) tr[1] |= (last ? 2ull : 1ull) << 32;
           __threadfence();
           *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
         }
@@ -351,25 +362,40 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         // barrier of a later cut tile, i.e. after every thread has read it)
         finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
         if (finish) {
-          // accumulator += every other contributor's part
+          // accumulator = sum of all parts in ascending contributor order
+          // (this CTA's own part taken from TMEM at its place), so the result
+          // does not depend on which contributor arrived last
 #pragma unroll 1
           for (int ch = 0; ch < kTileN / 32; ++ch) {
+            uint32_t own[32];
+            tmem_ld32(t_row + ch * 32, own);
             uint32_t v[32];
-            tmem_ld32(t_row + ch * 32, v);
             if (t < p.T) {
               for (int c = c_first; c <= c_last; ++c) {
-                if (c == static_cast<int>(blockIdx.x)) continue;
-                const float4* other =
-                    reinterpret_cast<const float4*>(ws_slot(p, c, c == c_first ? 1 : 0));
+                float part[32];
+                if (c == static_cast<int>(blockIdx.x)) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 q = __ldcg(other + (ch * 8 + j) * kTileM + row);
-                  v[4 * j] = __float_as_uint(f32(v[4 * j]) + q.x);
-                  v[4 * j + 1] = __float_as_uint(f32(v[4 * j + 1]) + q.y);
-                  v[4 * j + 2] = __float_as_uint(f32(v[4 * j + 2]) + q.z);
-                  v[4 * j + 3] = __float_as_uint(f32(v[4 * j + 3]) + q.w);
+                  for (int e = 0; e < 32; ++e) part[e] = f32(own[e]);
+                } else {
+                  const float4* other =
+                      reinterpret_cast<const float4*>(ws_slot(p, c, c == c_first ? 1 : 0));
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const float4 q = __ldcg(other + (ch * 8 + j) * kTileM + row);
+                    part[4 * j] = q.x;
+                    part[4 * j + 1] = q.y;
+                    part[4 * j + 2] = q.z;
+                    part[4 * j + 3] = q.w;
+                  }
                 }
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  v[e] = c == c_first ? __float_as_uint(part[e])
+                                      : __float_as_uint(f32(v[e]) + part[e]);
               }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = own[e];
             }
             __syncwarp();
             tmem_st32(t_row + ch * 32, v);
@@ -496,6 +522,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // accumulator fully read: hand it back to the MMA warp
       tc_fence_before();
       __syncwarp();
+      if (tr != nullptr) tr[3] = global_timer_ns();
       if (lane == 0) mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
       if (++acc == 2) {
         acc = 0;
@@ -508,6 +535,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (trace != nullptr && threadIdx.x == 0) {
+    trace[1] = global_timer_ns();
+    WorkIter it = work_begin(p);
+    int tile, kb0, kb1, n = 0;
+    while (work_next(p, it, tile, kb0, kb1)) ++n;
+    trace[2] = static_cast<uint64_t>(n);
+  }
 }
 
 template <typename E, int D, bool kBias>

@@ -29,6 +29,7 @@ struct WriteParams {
   // finished by whichever contributor arrives last (no CTA waits for another)
   int32_t dp_tiles;
   int64_t sk_units;
+  uint64_t* trace;              // null, or [gridDim.x][kTraceWords] timeline stamps
   float* workspace;             // [gridDim.x][2][kTileN/4][kTileM][4] fp32 partial tiles
   int32_t* counters;            // [gridDim.x] arrivals per cut tile, reset by the last one
   uint64_t wait_limit_ns;       // bound on any single in-kernel wait
@@ -46,6 +47,8 @@ constexpr int kStages = 4;
 constexpr int kTiledThreads = 192;
 constexpr int kGroupM = 8;     // m-blocks per raster group (L2 reuse of weight tiles)
 
+constexpr int kTraceWords = 64;      // per CTA: start, end, items, then 4 words per work item
+constexpr int kTraceItems = (kTraceWords - 3) / 4;
 constexpr int kMinUnitsPerCta = 8;   // k-blocks: keeps small problems from over-splitting
 
 size_t tiled_smem_bytes();

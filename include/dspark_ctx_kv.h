@@ -185,6 +185,14 @@ DSPARK_API int dspark_get_device_status(dspark_bundle_t bundle, void* stream, ui
 /* Reset the device status word to 0 (stream-ordered, asynchronous). */
 DSPARK_API int dspark_clear_device_status(dspark_bundle_t bundle, void* stream);
 
+/* Diagnostics: make later writes with this bundle record a per-CTA timeline
+ * into `buf` (device, uint64 [SMs x 64]: globaltimer ns at CTA start and end,
+ * the number of work items, then per work item its tile, its k-block range and
+ * kind, and the times its accumulator became ready and was released).  `words`
+ * is the buffer length; NULL turns tracing off (the default).  Tracing adds a
+ * few global stores per work item and does not change results. */
+DSPARK_API int dspark_set_trace_buffer(dspark_bundle_t bundle, uint64_t* buf, int64_t words);
+
 DSPARK_API int dspark_bundle_get_info(dspark_bundle_t bundle, dspark_bundle_info* info /* (host) */);
 
 /* Release the bundle's device memory (synchronises the device first). NULL is a no-op. */
