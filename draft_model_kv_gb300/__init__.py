@@ -20,7 +20,8 @@ from ._abi import (DSparkError, FLAG_LOC_RANGE, FLAG_POS_RANGE, FLAG_TIMEOUT,  #
 __all__ = [
     "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
-    "dspark_status_string", "dspark_set_trace_buffer", "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
+    "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
+    "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
 
@@ -188,3 +189,56 @@ def dspark_set_trace_buffer(bundle: Bundle, buf) -> None:
     else:
         code = load().dspark_set_trace_buffer(bundle.handle, buf.data_ptr(), buf.numel())
     _abi.check(code, "dspark_set_trace_buffer")
+
+
+def dspark_write_ctx_kv_noalloc(stacked_weight, k_norm_weight, eps: float, num_layers: int,
+                                num_kv_heads: int, head_dim: int, ctx_hidden, positions, cos_sin,
+                                cache_loc, k_pools, v_pools, stacked_bias=None, commit_lens=None,
+                                loc_row_width: Optional[int] = None, status_flags=None,
+                                stream=None) -> None:
+    """The write for callers that must not allocate device memory.
+
+    For frameworks whose own allocator owns all device memory, or loops that
+    cannot afford cudaMalloc's device-wide synchronisation.  The caller passes
+    the stacked weight [N, hidden] (rows l0:K, l0:V, l1:K, ...), the fp32
+    k_norm weights [num_layers, head_dim], optional stacked bias [N], every
+    input and the pools; the kernel's scratch lives in a fixed 16 MiB + 4 KiB
+    device array inside the library (at most 64 SMs per call).  Calls share
+    that array, so calls whose kernels overlap on the GPU race: keep them
+    ordered.  Make the first call on a device before any stream capture.
+    """
+    import torch
+    T = ctx_hidden.shape[0]
+    if stacked_weight.dim() != 2 or stacked_weight.stride(1) != 1:
+        raise ValueError("stacked_weight must be [N, hidden] with unit column stride")
+    if k_norm_weight.dtype != torch.float32 or not k_norm_weight.is_contiguous():
+        raise TypeError("k_norm_weight must be a contiguous float32 [num_layers, head_dim] tensor")
+    if ctx_hidden.dim() != 2 or (T > 0 and ctx_hidden.stride(1) != 1):
+        raise ValueError("ctx_hidden must be [T, hidden] with unit column stride")
+    for name, t, dt in (("positions", positions, torch.int64), ("cache_loc", cache_loc, torch.int64),
+                        ("cos_sin", cos_sin, torch.float32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous {dt} tensor")
+    if commit_lens is not None and (commit_lens.dtype != torch.int32 or not commit_lens.is_contiguous()):
+        raise TypeError("commit_lens must be a contiguous int32 tensor")
+    if len(k_pools) != num_layers or len(v_pools) != num_layers:
+        raise ValueError("one K and one V pool per layer")
+    dt = stacked_weight.dtype
+    for t in [ctx_hidden] + list(k_pools) + list(v_pools) + ([] if stacked_bias is None else [stacked_bias]):
+        if t.dtype != dt:
+            raise TypeError("weights, hidden, bias and pools must share one dtype")
+    slots = k_pools[0].shape[0]
+    width = 0 if loc_row_width is None else int(loc_row_width)
+    nwin = 0 if commit_lens is None else commit_lens.numel()
+    kstr = (ctypes.c_int64 * num_layers)(*[p.stride(0) for p in k_pools])
+    vstr = (ctypes.c_int64 * num_layers)(*[p.stride(0) for p in v_pools])
+    code = load().dspark_write_ctx_kv_noalloc(
+        stacked_weight.data_ptr(), stacked_weight.stride(0),
+        None if stacked_bias is None else stacked_bias.data_ptr(), k_norm_weight.data_ptr(),
+        eps, num_layers, stacked_weight.shape[1], num_kv_heads, head_dim, _dtype_code(dt),
+        ctx_hidden.data_ptr(), T, ctx_hidden.stride(0) if T > 0 else ctx_hidden.shape[1],
+        positions.data_ptr(), cos_sin.data_ptr(), cos_sin.shape[0], cache_loc.data_ptr(),
+        None if commit_lens is None else commit_lens.data_ptr(), width, nwin,
+        _ptr_array(k_pools), _ptr_array(v_pools), kstr, vstr, slots,
+        None if status_flags is None else status_flags.data_ptr(), _stream_handle(stream))
+    _abi.check(code, "dspark_write_ctx_kv_noalloc")

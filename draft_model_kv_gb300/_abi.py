@@ -26,6 +26,7 @@ STATUS = {
     5: "E_DTYPE_MISMATCH", 6: "E_SHAPE_MISMATCH", 7: "E_HEAD_DIM", 8: "E_BIAS_MISMATCH",
     9: "E_COMMIT_ARGS", 10: "E_NUMEL", 11: "E_ALIGNMENT", 12: "E_POOL_LAYOUT",
     13: "E_TOO_MANY_LAYERS", 14: "E_DEVICE", 15: "E_CUDA", 16: "E_DEVICE_FAULT",
+    17: "E_SCRATCH_LIMIT",
 }
 CODE = {v: k for k, v in STATUS.items()}
 
@@ -33,6 +34,7 @@ EXPORTS = (
     "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv", "dspark_write_ctx_kv",
     "dspark_get_device_status", "dspark_clear_device_status", "dspark_bundle_get_info",
     "dspark_free_bundle", "dspark_status_string", "dspark_set_trace_buffer",
+    "dspark_write_ctx_kv_noalloc",
 )
 
 
@@ -92,6 +94,12 @@ def load() -> ctypes.CDLL:
     lib.dspark_bundle_get_info.restype = ctypes.c_int
     lib.dspark_free_bundle.argtypes = [vp]
     lib.dspark_free_bundle.restype = None
+    lib.dspark_write_ctx_kv_noalloc.argtypes = [
+        vp, i64, vp, vp, ctypes.c_float, i32, i32, i32, i32, i32,
+        vp, i64, i64, vp, vp, i64, vp, vp, i64, i64,
+        ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64), ctypes.POINTER(i64), i64,
+        vp, vp]
+    lib.dspark_write_ctx_kv_noalloc.restype = ctypes.c_int
     lib.dspark_set_trace_buffer.argtypes = [vp, vp, i64]
     lib.dspark_set_trace_buffer.restype = ctypes.c_int
     lib.dspark_status_string.argtypes = [ctypes.c_int]

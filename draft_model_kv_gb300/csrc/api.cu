@@ -121,6 +121,7 @@ const char* dspark_status_string(int code) {
     case DSPARK_E_DEVICE: return "no sm_103 device, or not the bundle's device";
     case DSPARK_E_CUDA: return "CUDA runtime error";
     case DSPARK_E_DEVICE_FAULT: return "device-side check fired";
+    case DSPARK_E_SCRATCH_LIMIT: return "launch needs more scratch than the no-alloc entry point's static array holds";
     default: return "unknown status";
   }
 }

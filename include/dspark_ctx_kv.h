@@ -69,7 +69,9 @@ typedef enum dspark_status {
   DSPARK_E_TOO_MANY_LAYERS = 13,  /* num_layers > DSPARK_MAX_LAYERS */
   DSPARK_E_DEVICE = 14,           /* no sm_103 device, or not the bundle's device */
   DSPARK_E_CUDA = 15,             /* a CUDA runtime call failed */
-  DSPARK_E_DEVICE_FAULT = 16      /* a device-side check fired (see status flags) */
+  DSPARK_E_DEVICE_FAULT = 16,     /* a device-side check fired (see status flags) */
+  DSPARK_E_SCRATCH_LIMIT = 17     /* dspark_write_ctx_kv_noalloc: the launch would need more
+                                     scratch than the library's static array holds */
 } dspark_status;
 
 #define DSPARK_MAX_LAYERS 32
@@ -176,6 +178,52 @@ DSPARK_API int dspark_write_ctx_kv(dspark_bundle_t bundle,
                         const int64_t* k_row_strides, const int64_t* v_row_strides,
                         int32_t pool_dtype, int64_t pool_slots,
                         void* stream);
+
+/*
+ * dspark_write_ctx_kv_noalloc -- the same write for callers that must not
+ * allocate device memory.  (The pages have no counterpart: their write always
+ * runs inside a serving framework that allocates freely.)
+ *
+ * Some callers cannot call cudaMalloc: frameworks whose own pool allocator
+ * owns all device memory (an allocation behind its back escapes its accounting
+ * and can fragment or exhaust the pool), and latency-critical loops that
+ * cannot afford cudaMalloc's implicit device-wide synchronisation.  They cannot
+ * use dspark_pack_ctx_kv either, since the bundle is allocated.  This entry
+ * point allocates nothing: the caller passes the stacked parameters the pack
+ * would build, every input and every output, and the kernel's scratch (the
+ * partial-tile workspace of the split schedule and its arrival counters) lives
+ * in a file-scope device array of 16 MiB + 4 KiB that the library reserves on
+ * every GPU it is loaded on, until the process exits.
+ *
+ *  stacked_weight    [N, hidden], N = num_layers*2*num_kv_heads*head_dim, rows
+ *                    l0:K, l0:V, l1:K, ... (the pack's layout), row stride
+ *                    weight_row_stride elements (16-byte pitch), 16-byte aligned
+ *  stacked_bias      NULL or [N] in dtype
+ *  k_norm_weight     [num_layers, head_dim] fp32, 16-byte aligned
+ *  dtype             DSPARK_DTYPE_BF16 or DSPARK_DTYPE_FP16 (weights, hidden, pools)
+ *  status_flags      NULL, or a device uint32 the kernel ORs DSPARK_FLAG_* bits into
+ *  other arguments   as for dspark_write_ctx_kv
+ *
+ * A call runs on at most 64 SMs (the CTAs whose partial tiles fit in the
+ * array); a launch that would need more scratch is refused with
+ * DSPARK_E_SCRATCH_LIMIT.  All calls share the one array and it keeps the
+ * previous call's contents: each call clears the arrival counters (a
+ * stream-ordered memset) before its kernel, and two calls whose kernels
+ * overlap on the GPU race and give wrong results, so keep the calls on a
+ * device ordered.  The first call on each device looks up the array's address
+ * and sets the kernel's shared-memory limit; make that first call before any
+ * stream capture begins.
+ */
+DSPARK_API int dspark_write_ctx_kv_noalloc(
+    const void* stacked_weight, int64_t weight_row_stride, const void* stacked_bias,
+    const float* k_norm_weight, float eps, int32_t num_layers, int32_t hidden,
+    int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+    const void* ctx_hidden, int64_t num_tokens, int64_t hidden_row_stride,
+    const int64_t* positions, const float* cos_sin, int64_t max_pos,
+    const int64_t* cache_loc, const int32_t* commit_lens, int64_t loc_row_width,
+    int64_t num_windows, void* const* k_pools, void* const* v_pools,
+    const int64_t* k_row_strides, const int64_t* v_row_strides, int64_t pool_slots,
+    uint32_t* status_flags, void* stream);
 
 /* Copy the bundle's device status word (DSPARK_FLAG_* bits, OR-ed over all
  * writes since the last clear) to *flags, ordered after prior work on
