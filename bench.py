@@ -10,7 +10,8 @@ bf16, commit_lens truncation, 65536-slot pools).
 
 Prints ONE JSON line (rank 0).  `value` is device time: CUDA events on the
 launching stream around each step, inputs resident in HBM, the L2 flushed
-(256 MiB write) between steps outside the events.  `e2e` is the same metric
+(256 MiB write) between steps outside the events, and the step enqueued
+before its start event fires (a short device-side delay precedes it).  `e2e` is the same metric
 through the public API with pinned host inputs: host->device copies of the
 step's inputs, the write, and a device->host read of the status word, timed
 on the host.  `--impl reference` times the CPU oracle instead (the reference
@@ -34,6 +35,7 @@ if ROOT not in sys.path:
 METRIC = "ctx-KV tokens/s (stacked proj+norm+RoPE+pool write); % of roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+SLEEP_CYCLES = 200_000          # ~0.1 ms of GPU time between the L2 flush and a timed step
 
 
 def peaks():
@@ -249,6 +251,9 @@ def run_gpu(args, w):
     with ClockSampler(local) as clk:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
+            # a short device-side delay lets the host enqueue the step before its
+            # start event fires, so the events bracket device work only
+            torch.cuda._sleep(SLEEP_CYCLES)
             starts[i].record(stream)
             step()
             ends[i].record(stream)

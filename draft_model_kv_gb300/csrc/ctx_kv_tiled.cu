@@ -6,13 +6,17 @@
 // PR #31986 summary page, _stacked_ctx_kv_params).  256 columns are whole
 // heads (D = 64 or 128), so each tile's epilogue can finish its heads alone.
 //
-//   warp 0      TMA producer: X and W_all K-slices into a 4-stage smem ring
-//   warp 1      MMA issuer: tcgen05.mma 128x256x16 into one of two TMEM
-//               accumulators (2 x 256 fp32 columns); owns TMEM alloc/free
-//   warps 2..5  epilogue: each thread owns one token row of the accumulator
+//   warps 0..7  epilogue, two warpgroups that take alternate heads of a tile:
+//               each thread owns one token row of the accumulator
 //               (tcgen05.ld 32x32b), so the RMSNorm sum of squares is a
 //               per-thread sum and the neox pair (i, i + D/2) sits in the same
-//               thread's registers; then 16-byte stores into the pool row.
+//               thread's registers; then 16-byte stores into the pool row
+//   warp 8      TMA producer: X and W_all K-slices into a 4-stage smem ring
+//   warp 9      MMA issuer: tcgen05.mma 128x256x16 into one of two TMEM
+//               accumulators (2 x 256 fp32 columns); owns TMEM alloc/free
+//   warps 10,11 idle (they complete the control warpgroup)
+// Registers are moved to the epilogue with setmaxnreg (control warpgroup 40,
+// epilogue warpgroups 232 per thread).
 //
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
 // Per-token rules (sglang PR #31847 summary page, fused_kv_norm_rope_write):
@@ -41,6 +45,7 @@ struct ElemOps<__nv_bfloat16> {
   __device__ static __forceinline__ float load(const void* p, int64_t i) {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
   }
+  __device__ static __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
 template <>
@@ -53,12 +58,22 @@ struct ElemOps<__half> {
   __device__ static __forceinline__ float load(const void* p, int64_t i) {
     return __half2float(reinterpret_cast<const __half*>(p)[i]);
   }
+  __device__ static __forceinline__ float to_float(__half v) { return __half2float(v); }
 };
 
 constexpr uint32_t kStageBytesA = kTileM * kTileK * 2;   // 16 KB
 constexpr uint32_t kStageBytesB = kTileN * kTileK * 2;   // 32 KB
 constexpr uint32_t kAccCols = kTileN;                    // fp32 columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;             // double buffer = 512 (all of TMEM)
+constexpr int kEpiWarps = 8;                             // two epilogue warpgroups
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kRegsControl = 40;
+constexpr uint32_t kRegsEpilogue = 232;
+static_assert(kTiledThreads == 384, "three warpgroups");
+static_assert(128 * kRegsControl + 256 * kRegsEpilogue == 384 * kLaunchRegs,
+              "the register split must use exactly the launch allocation");
 
 struct SmemBarriers {
   uint64_t full[kStages];
@@ -88,25 +103,44 @@ __device__ __forceinline__ void flag(const WriteParams& p, uint32_t bits) {
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
-// Store 32 consecutive outputs (already rounded/packed in pairs) as 4 x 16 B.
-__device__ __forceinline__ void store32(void* dst, const uint32_t (&w)[16]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// 8 consecutive 16-bit values (one 16-byte load) widened to fp32.
+template <typename E>
+__device__ __forceinline__ void load8(const void* base, int64_t idx, float (&out)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(reinterpret_cast<const E*>(base) + idx);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  for (int i = 0; i < 4; ++i) {
+    const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFFu), hi = static_cast<uint16_t>(w[i] >> 16);
+    E a, b;
+    memcpy(&a, &lo, 2);
+    memcpy(&b, &hi, 2);
+    out[2 * i] = ElemOps<E>::to_float(a);
+    out[2 * i + 1] = ElemOps<E>::to_float(b);
+  }
+}
+
+// 16-byte store of 8 packed 16-bit outputs.
+__device__ __forceinline__ void st16(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
 }
 
 // Work of one CTA: first its whole tiles of the data-parallel waves, then its
-// contiguous range of the stream-K k-block space.
+// contiguous range of the stream-K k-block space, walked from its end back to
+// its start.  The backward walk makes a CTA begin with the (usually small)
+// first k-blocks of the tile at the end of its range, publish that part while
+// it computes the rest, and end with the (usually large) last part of the tile
+// at the start of its range, which it then finishes itself: the partial tile
+// it holds in TMEM is the last to arrive.
 struct WorkIter {
   int dp_tile;
-  int64_t cur, end;
+  int64_t start, cur;
 };
 
 __device__ __forceinline__ WorkIter work_begin(const WriteParams& p) {
   WorkIter it;
   it.dp_tile = blockIdx.x;
-  it.cur = static_cast<int64_t>(blockIdx.x) * p.sk_units / gridDim.x;
-  it.end = static_cast<int64_t>(blockIdx.x + 1) * p.sk_units / gridDim.x;
+  it.start = static_cast<int64_t>(blockIdx.x) * p.sk_units / gridDim.x;
+  it.cur = static_cast<int64_t>(blockIdx.x + 1) * p.sk_units / gridDim.x;
   return it;
 }
 
@@ -119,12 +153,13 @@ __device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, in
     it.dp_tile += gridDim.x;
     return true;
   }
-  if (it.cur < it.end) {
-    const int64_t t = it.cur / p.num_kb;
-    kb0 = static_cast<int>(it.cur - t * p.num_kb);
-    const int64_t rem = it.end - it.cur;
-    kb1 = rem < static_cast<int64_t>(p.num_kb - kb0) ? kb0 + static_cast<int>(rem) : p.num_kb;
-    it.cur += kb1 - kb0;
+  if (it.cur > it.start) {
+    const int64_t t = (it.cur - 1) / p.num_kb;
+    const int64_t tile_start = t * p.num_kb;
+    const int64_t lo = it.start > tile_start ? it.start : tile_start;
+    kb0 = static_cast<int>(lo - tile_start);
+    kb1 = static_cast<int>(it.cur - tile_start);
+    it.cur = lo;
     tile = p.dp_tiles + static_cast<int>(t);
     return true;
   }
@@ -169,17 +204,17 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->tmem_full[b]), 1);
-      mbar_init(smem_u32(&bars->tmem_empty[b]), 4);   // one arrival per epilogue warp
+      mbar_init(smem_u32(&bars->tmem_empty[b]), kEpiWarps);   // one arrival per epilogue warp
     }
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_w);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -190,114 +225,122 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   uint64_t* trace = p.trace != nullptr ? p.trace + static_cast<size_t>(blockIdx.x) * kTraceWords : nullptr;
   if (trace != nullptr && threadIdx.x == 0) trace[0] = global_timer_ns();
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_last();
-      const uint64_t pol_x = l2_policy_evict_normal();
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t uses[kStages] = {};
-      bool ok = true;
-      WorkIter it = work_begin(p);
-      int tile, kb0, kb1;
-      while (ok && work_next(p, it, tile, kb0, kb1)) {
-        int m_blk, n_blk;
-        tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns)) {
-            ok = false;
-            break;
-          }
-          const uint32_t full = smem_u32(&bars->full[stage]);
-          mbar_arrive_expect_tx(full, kStageBytesA + kStageBytesB);
-          tma_load_2d(smem_u32(smem_a + stage * kStageBytesA), &tmap_x, kb * kTileK,
-                      m_blk * kTileM, full, pol_x);
-          tma_load_2d(smem_u32(smem_b + stage * kStageBytesB), &tmap_w, kb * kTileK,
-                      n_blk * kTileN, full, pol_w);
-          ++uses[stage];
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+  if (warp >= kEpiWarps) {
+    regs_decrease<kRegsControl>();
+    if (warp == kProducerWarp) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        const uint64_t pol_w = l2_policy_evict_last();
+        const uint64_t pol_x = l2_policy_evict_normal();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t uses[kStages] = {};
+        bool ok = true;
+        WorkIter it = work_begin(p);
+        int tile, kb0, kb1;
+        while (ok && work_next(p, it, tile, kb0, kb1)) {
+          int m_blk, n_blk;
+          tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = smem_u32(&bars->full[stage]);
+            mbar_arrive_expect_tx(full, kStageBytesA + kStageBytesB);
+            tma_load_2d(smem_u32(smem_a + stage * kStageBytesA), &tmap_x, kb * kTileK,
+                        m_blk * kTileM, full, pol_x);
+            tma_load_2d(smem_u32(smem_b + stage * kStageBytesB), &tmap_w, kb * kTileK,
+                        n_blk * kTileN, full, pol_w);
+            ++uses[stage];
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        flag(p, DSPARK_FLAG_TIMEOUT);
-      }
-      // every load issued must land before the CTA may exit (bounded by time
-      // only: an abort must not cut this wait short)
-      int never = 0;
+        if (!ok) {
+          *abort_flag = 1;
+          flag(p, DSPARK_FLAG_TIMEOUT);
+        }
+        // every load issued must land before the CTA may exit (bounded by time
+        // only: an abort must not cut this wait short)
+        int never = 0;
 #pragma unroll
-      for (int s = 0; s < kStages; ++s)
-        if (uses[s] > 0) mbar_wait(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = f16_instr_desc(ElemOps<E>::kFmt, kTileM, kTileN);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      bool issued = false;
-      WorkIter it = work_begin(p);
-      int tile, kb0, kb1;
-      while (ok && work_next(p, it, tile, kb0, kb1)) {
-        if (!mbar_wait(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort_flag,
-                       p.wait_limit_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&bars->full[stage]), phase, abort_flag, p.wait_limit_ns)) {
+        for (int s = 0; s < kStages; ++s)
+          if (uses[s] > 0) mbar_wait(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
+      }
+    } else if (warp == kMmaWarp) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc = f16_instr_desc(ElemOps<E>::kFmt, kTileM, kTileN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        bool issued = false;
+        WorkIter it = work_begin(p);
+        int tile, kb0, kb1;
+        while (ok && work_next(p, it, tile, kb0, kb1)) {
+          if (!mbar_wait(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort_flag,
+                         p.wait_limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem_a + stage * kStageBytesA);
-          const uint32_t b0 = smem_u32(smem_b + stage * kStageBytesB);
+          const uint32_t d_tmem = tmem_base + acc * kAccCols;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(smem_u32(&bars->full[stage]), phase, abort_flag, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem_a + stage * kStageBytesA);
+            const uint32_t b0 = smem_u32(smem_b + stage * kStageBytesB);
 #pragma unroll
-          for (int k = 0; k < kTileK / 16; ++k) {
-            // advancing 16 elements along K = 32 bytes inside the swizzle atom
-            umma_f16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
-                     idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            for (int k = 0; k < kTileK / 16; ++k) {
+              // advancing 16 elements along K = 32 bytes inside the swizzle atom
+              umma_f16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
+                       idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            }
+            issued = true;
+            umma_commit(smem_u32(&bars->empty[stage]));
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          issued = true;
-          umma_commit(smem_u32(&bars->empty[stage]));
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+          if (!ok) break;
+          umma_commit(smem_u32(&bars->tmem_full[acc]));
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
           }
         }
-        if (!ok) break;
-        umma_commit(smem_u32(&bars->tmem_full[acc]));
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
+        if (!ok) {
+          *abort_flag = 1;
+          flag(p, DSPARK_FLAG_TIMEOUT);
         }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        flag(p, DSPARK_FLAG_TIMEOUT);
-      }
-      if (issued) {
-        // all MMAs issued by this thread complete before TMEM is released
-        umma_commit(smem_u32(&bars->drain));
-        int never = 0;
-        mbar_wait(smem_u32(&bars->drain), 0, &never, p.wait_limit_ns);
+        if (issued) {
+          // all MMAs issued by this thread complete before TMEM is released
+          umma_commit(smem_u32(&bars->drain));
+          int never = 0;
+          mbar_wait(smem_u32(&bars->drain), 0, &never, p.wait_limit_ns);
+        }
       }
     }
   } else {
+    regs_increase<kRegsEpilogue>();
     // ------------------------------------------------------------ epilogue
     constexpr int kHalf = D / 2;
-    const int quarter = warp % 4;                 // TMEM lanes this warp may read
-    const int row = quarter * 32 + lane;          // token row inside the tile
-    const int etid = threadIdx.x - 64;            // 0..127 among the epilogue threads
+    constexpr int kChunks = kTileN / 32;            // 32-column chunks of a tile
+    const int group = warp / 4;                     // warpgroup 0 or 1
+    const int quarter = warp % 4;                   // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;            // token row inside the tile
+    const int etid = threadIdx.x;                   // 0..255 among the epilogue threads
+    const int ch_lo = group * (kChunks / 2);        // this group's chunks of a cut tile
+    const int ch_hi = ch_lo + kChunks / 2;
     int acc = 0;
     uint32_t acc_phase = 0;
     int item = 0;
@@ -306,25 +349,63 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     while (work_next(p, it, tile, kb0, kb1)) {
       int m_blk, n_blk;
       tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+      bool final_item;
+      {
+        WorkIter peek = it;
+        int t2, a2, b2;
+        final_item = !work_next(p, peek, t2, a2, b2);
+      }
+      // ---- per-token decision (same for every head of the tile); it does not
+      // depend on the accumulator, so it runs while the MMAs are in flight
+      const int64_t t = static_cast<int64_t>(m_blk) * kTileM + row;
+      bool write = false;
+      int64_t loc = 0, pos = 0;
+      if (t < p.T) {
+        loc = p.cache_loc[t];
+        write = loc >= 0;
+        if (write && p.loc_row_width > 0) {
+          const int64_t b = t / p.loc_row_width;
+          if (t - b * p.loc_row_width >= static_cast<int64_t>(p.commit_lens[b])) write = false;
+        }
+        if (write) {
+          pos = p.positions[t];
+          if (pos < 0 || pos >= p.max_pos) {
+            if (group == 0) flag(p, DSPARK_FLAG_POS_RANGE);
+            write = false;
+          } else if (loc >= p.pool_slots) {
+            if (group == 0) flag(p, DSPARK_FLAG_LOC_RANGE);
+            write = false;
+          }
+        }
+      }
+      if (write) {
+        // the K heads of this tile will read this token's cos/sin row
+        const char* cs_row = reinterpret_cast<const char*>(p.cos_sin + pos * D);
+        for (int b = group * 128; b < D * 4; b += 256) prefetch_l2(cs_row + b);
+      }
       // the outcome must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort_flag,
                                  p.wait_limit_ns);
-      uint64_t* tr = (trace != nullptr && etid == 0 && item < kTraceItems) ? trace + 3 + 4 * item : nullptr;
+      // stamps come from the thread of row 0 of the first group
+      uint64_t* tr =
+          (trace != nullptr && etid == 0 && item < kTraceItems) ? trace + 3 + 6 * item : nullptr;
       if (tr != nullptr) {
         tr[0] = static_cast<uint64_t>(tile);
         tr[1] = (static_cast<uint64_t>(kb0) << 16) | static_cast<uint64_t>(kb1);
         tr[2] = global_timer_ns();
+        tr[3] = tr[4] = 0;
       }
       ++item;
-      if (!__all_sync(0xffffffffu, got)) {
-        if (lane == 0) {
+      // every epilogue warp takes the same decision (they meet at named
+      // barriers below), and every wait ends within its time bound
+      if (!named_barrier_and(1, kEpiThreads, got)) {
+        if (etid == 0) {
           *abort_flag = 1;
           flag(p, DSPARK_FLAG_TIMEOUT);
         }
         break;
       }
       tc_fence_after();
-      const int64_t t = static_cast<int64_t>(m_blk) * kTileM + row;
       const uint32_t t_row = tmem_base + acc * kAccCols + (static_cast<uint32_t>(quarter * 32) << 16);
 
       // ---- a tile cut between CTAs: publish this part; the last contributor
@@ -334,100 +415,148 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
         const int c_first = sk_owner(p, u0);
         const int c_last = sk_owner(p, u0 + p.num_kb - 1);
-        float4* mine = reinterpret_cast<float4*>(ws_slot(p, blockIdx.x, kb0 > 0 ? 0 : 1));
-#pragma unroll 1
-        for (int ch = 0; ch < kTileN / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(t_row + ch * 32, v);
-          if (t < p.T) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              __stcg(mine + (ch * 8 + j) * kTileM + row,
-                     make_float4(f32(v[4 * j]), f32(v[4 * j + 1]), f32(v[4 * j + 2]), f32(v[4 * j + 3])));
+        const int me = static_cast<int>(blockIdx.x);
+        // If every other contributor has already published (the usual case for
+        // a CTA's last work item), this CTA finishes the tile without
+        // publishing its own part.  An earlier item of a CTA is almost never
+        // the last to arrive, so it skips the check.
+        finish = false;
+        if (final_item) {
+          if (etid == 0) {
+            const int seen = ld_acquire_gpu(p.counters + c_last);
+            const int done = seen == c_last - c_first;
+            if (done) p.counters[c_last] = 0;   // no other contributor touches it again
+            *reinterpret_cast<volatile int*>(&bars->last_arrival) = done;
           }
-          __syncwarp();
+          named_barrier(1, kEpiThreads);
+          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
+          named_barrier(1, kEpiThreads);
         }
-        __threadfence();
-        named_barrier(1, 128);
-        if (etid == 0) {
-          const int old = atomicAdd(p.counters + c_last, 1);
-          const int last = old == c_last - c_first;
-          if (last) p.counters[c_last] = 0;   // ready for the next launch
-          if (tr != nullptr) tr[1] |= (last ? 2ull : 1ull) << 32;
-          __threadfence();
-          *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
-        }
-        named_barrier(1, 128);
-        // (the flag is next written only after all 128 threads pass the first
-        // barrier of a later cut tile, i.e. after every thread has read it)
-        finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
-        if (finish) {
-          // accumulator = sum of all parts in ascending contributor order
-          // (this CTA's own part taken from TMEM at its place), so the result
-          // does not depend on which contributor arrived last
+        if (!finish) {
+          float4* mine = reinterpret_cast<float4*>(ws_slot(p, me, kb0 > 0 ? 0 : 1));
 #pragma unroll 1
-          for (int ch = 0; ch < kTileN / 32; ++ch) {
-            uint32_t own[32];
-            tmem_ld32(t_row + ch * 32, own);
-            uint32_t v[32];
+          for (int ch = ch_lo; ch < ch_hi; ch += 2) {
+            uint32_t v[32], u[32];
+            tmem_ld32x2(t_row + ch * 32, t_row + (ch + 1) * 32, v, u);
             if (t < p.T) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                __stcg(mine + (ch * 8 + j) * kTileM + row,
+                       make_float4(f32(v[4 * j]), f32(v[4 * j + 1]), f32(v[4 * j + 2]), f32(v[4 * j + 3])));
+                __stcg(mine + ((ch + 1) * 8 + j) * kTileM + row,
+                       make_float4(f32(u[4 * j]), f32(u[4 * j + 1]), f32(u[4 * j + 2]), f32(u[4 * j + 3])));
+              }
+            }
+            __syncwarp();
+          }
+          if (tr != nullptr) tr[3] = global_timer_ns();   // dump issued
+          __threadfence();
+          named_barrier(1, kEpiThreads);
+          if (tr != nullptr) tr[4] = global_timer_ns();   // dump visible
+          if (etid == 0) {
+            const int old = atomicAdd(p.counters + c_last, 1);
+            const int last = old == c_last - c_first;
+            if (last) p.counters[c_last] = 0;   // ready for the next launch
+            __threadfence();
+            *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
+          }
+          named_barrier(1, kEpiThreads);
+          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
+          named_barrier(1, kEpiThreads);
+        }
+        if (tr != nullptr) {
+          tr[1] |= (finish ? 2ull : 1ull) << 32;
+          if (finish) tr[3] = global_timer_ns();
+        }
+        if (finish) {
+          // accumulator = sum of all parts in ascending contributor order (this
+          // CTA's own part taken from TMEM at its place), so the result does not
+          // depend on which contributor arrived last.  Each group sums its half
+          // of the columns.
+          const int64_t rows_left = static_cast<int64_t>(p.T) - static_cast<int64_t>(m_blk) * kTileM;
+          const int rv = rows_left < kTileM ? static_cast<int>(rows_left) : kTileM;
+          const int n_oth = c_last - c_first;
+          // After the CTA's last MMA the operand ring is idle: the other parts
+          // are staged there (each group in its own half) with many asynchronous
+          // 16-byte copies in flight; each thread copies, then reads, only its
+          // own row.  Otherwise they are read from the workspace directly.
+          constexpr int kHalfRingF4 = kStages * (kStageBytesA + kStageBytesB) / 32;
+          const int per_chunk = n_oth * 8 * rv;           // float4 per column chunk
+          const bool staged = final_item && per_chunk <= kHalfRingF4;
+          int cpr = kChunks / 2;
+          if (staged && per_chunk > 0) {
+            cpr = kHalfRingF4 / per_chunk;                 // >= 1 here
+            cpr = cpr > kChunks / 2 ? kChunks / 2 : cpr;
+          }
+          const uint32_t ring = smem_u32(smem) + group * kHalfRingF4 * 16;
+          const float4* ring_f4 = reinterpret_cast<const float4*>(smem) + group * kHalfRingF4;
+#pragma unroll 1
+          for (int ch0 = ch_lo; ch0 < ch_hi; ch0 += cpr) {
+            const int nch = (ch_hi - ch0) < cpr ? (ch_hi - ch0) : cpr;
+            if (staged && row < rv) {
+              int oi = 0;
               for (int c = c_first; c <= c_last; ++c) {
-                float part[32];
-                if (c == static_cast<int>(blockIdx.x)) {
+                if (c == me) continue;
+                const float4* src =
+                    reinterpret_cast<const float4*>(ws_slot(p, c, c == c_first ? 1 : 0));
+                for (int cl = 0; cl < nch; ++cl)
 #pragma unroll
-                  for (int e = 0; e < 32; ++e) part[e] = f32(own[e]);
+                  for (int j = 0; j < 8; ++j)
+                    cp_async16(ring + 16u * static_cast<uint32_t>(((oi * nch + cl) * 8 + j) * rv + row),
+                               src + ((ch0 + cl) * 8 + j) * kTileM + row);
+                ++oi;
+              }
+              cp_async_wait_all();
+            }
+            const int stride = staged ? rv : kTileM;     // float4 between column groups
+#pragma unroll 1
+            for (int cl = 0; cl < nch; ++cl) {
+              const int ch = ch0 + cl;
+              uint32_t v[32];
+              int oi = 0;
+              for (int c = c_first; c <= c_last; ++c) {
+                uint32_t part[32];
+                if (c == me) {
+                  tmem_ld32(t_row + ch * 32, part);   // warp-uniform branch
                 } else {
-                  const float4* other =
-                      reinterpret_cast<const float4*>(ws_slot(p, c, c == c_first ? 1 : 0));
+                  if (row < rv) {
+                    const float4* src =
+                        staged ? ring_f4 + (oi * nch + cl) * 8 * rv + row
+                               : reinterpret_cast<const float4*>(ws_slot(p, c, c == c_first ? 1 : 0)) +
+                                     ch * 8 * kTileM + row;
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    const float4 q = __ldcg(other + (ch * 8 + j) * kTileM + row);
-                    part[4 * j] = q.x;
-                    part[4 * j + 1] = q.y;
-                    part[4 * j + 2] = q.z;
-                    part[4 * j + 3] = q.w;
+                    for (int j = 0; j < 8; ++j) {
+                      const float4 q = src[j * stride];
+                      part[4 * j] = __float_as_uint(q.x);
+                      part[4 * j + 1] = __float_as_uint(q.y);
+                      part[4 * j + 2] = __float_as_uint(q.z);
+                      part[4 * j + 3] = __float_as_uint(q.w);
+                    }
+                  } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) part[e] = 0u;
                   }
+                  ++oi;
                 }
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                  v[e] = c == c_first ? __float_as_uint(part[e])
-                                      : __float_as_uint(f32(v[e]) + part[e]);
+                  v[e] = c == c_first ? part[e] : __float_as_uint(f32(v[e]) + f32(part[e]));
               }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = own[e];
+              __syncwarp();
+              tmem_st32(t_row + ch * 32, v);
             }
-            __syncwarp();
-            tmem_st32(t_row + ch * 32, v);
           }
+          // both groups' sums are in TMEM before any thread reads across halves
+          tc_fence_before();
+          named_barrier(1, kEpiThreads);
+          tc_fence_after();
         }
       }
 
+      if (tr != nullptr && finish) tr[4] = global_timer_ns();
       if (finish) {
-        // ---- per-token decision (same for every head of the tile)
-        bool write = false;
-        int64_t loc = 0, pos = 0;
-        if (t < p.T) {
-          loc = p.cache_loc[t];
-          write = loc >= 0;
-          if (write && p.loc_row_width > 0) {
-            const int64_t b = t / p.loc_row_width;
-            if (t - b * p.loc_row_width >= static_cast<int64_t>(p.commit_lens[b])) write = false;
-          }
-          if (write) {
-            pos = p.positions[t];
-            if (pos < 0 || pos >= p.max_pos) {
-              flag(p, DSPARK_FLAG_POS_RANGE);
-              write = false;
-            } else if (loc >= p.pool_slots) {
-              flag(p, DSPARK_FLAG_LOC_RANGE);
-              write = false;
-            }
-          }
-        }
-
 #pragma unroll 1
-        for (int seg = 0; seg < kTileN / D; ++seg) {
+        for (int seg = group; seg < kTileN / D; seg += 2) {
           const int c0 = n_blk * kTileN + seg * D;
           if (c0 >= p.N) break;
           const int layer = c0 / (2 * p.KV);
@@ -437,53 +566,85 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           const uint32_t t_seg = t_row + seg * D;
           if (is_v) {
             E* dst = reinterpret_cast<E*>(p.v_pool[layer]) + loc * p.v_stride[layer] + head * D;
-#pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-              uint32_t v[32];
-              tmem_ld32(t_seg + ch * 32, v);
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ch += 2) {
+              uint32_t v[32], u[32];
+              tmem_ld32x2(t_seg + ch * 32, t_seg + (ch + 1) * 32, v, u);
               if (write) {
-                uint32_t o[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                  float a = f32(v[e]), b = f32(v[e + 1]);
-                  if (kBias) {
-                    a += ElemOps<E>::load(p.bias, c0 + ch * 32 + e);
-                    b += ElemOps<E>::load(p.bias, c0 + ch * 32 + e + 1);
+                for (int q = 0; q < 4; ++q) {
+                  float x[8], y[8];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    x[e] = f32(v[8 * q + e]);
+                    y[e] = f32(u[8 * q + e]);
                   }
-                  o[e / 2] = ElemOps<E>::pack(a, b);
+                  if (kBias) {
+                    float bx[8], by[8];
+                    load8<E>(p.bias, c0 + ch * 32 + 8 * q, bx);
+                    load8<E>(p.bias, c0 + (ch + 1) * 32 + 8 * q, by);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                      x[e] += bx[e];
+                      y[e] += by[e];
+                    }
+                  }
+                  st16(dst + ch * 32 + 8 * q, ElemOps<E>::pack(x[0], x[1]), ElemOps<E>::pack(x[2], x[3]),
+                       ElemOps<E>::pack(x[4], x[5]), ElemOps<E>::pack(x[6], x[7]));
+                  st16(dst + (ch + 1) * 32 + 8 * q, ElemOps<E>::pack(y[0], y[1]),
+                       ElemOps<E>::pack(y[2], y[3]), ElemOps<E>::pack(y[4], y[5]),
+                       ElemOps<E>::pack(y[6], y[7]));
                 }
-                store32(dst + ch * 32, o);
               }
               __syncwarp();
             }
           } else {
             // RMSNorm: sum of squares over this thread's row of the head
             float ss = 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ch += 2) {
+              uint32_t v[32], u[32];
+              tmem_ld32x2(t_seg + ch * 32, t_seg + (ch + 1) * 32, v, u);
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-              uint32_t v[32];
-              tmem_ld32(t_seg + ch * 32, v);
+              for (int q = 0; q < 4; ++q) {
+                float bx[8], by[8];
+                if (kBias) {
+                  load8<E>(p.bias, c0 + ch * 32 + 8 * q, bx);
+                  load8<E>(p.bias, c0 + (ch + 1) * 32 + 8 * q, by);
+                }
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                float x = f32(v[e]);
-                if (kBias) x += ElemOps<E>::load(p.bias, c0 + ch * 32 + e);
-                ss = fmaf(x, x, ss);
+                for (int e = 0; e < 8; ++e) {
+                  float x = f32(v[8 * q + e]), y = f32(u[8 * q + e]);
+                  if (kBias) {
+                    x += bx[e];
+                    y += by[e];
+                  }
+                  ss = fmaf(x, x, ss);
+                  ss = fmaf(y, y, ss);
+                }
               }
             }
             const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
             const float* w = p.knorm + static_cast<int64_t>(layer) * D;
             const float* cs = p.cos_sin + pos * D;
             E* dst = reinterpret_cast<E*>(p.k_pool[layer]) + loc * p.k_stride[layer] + head * D;
-#pragma unroll
-            for (int hc = 0; hc < kHalf / 32; ++hc) {
-              uint32_t a[32], b[32];
-              tmem_ld32(t_seg + hc * 32, a);
-              tmem_ld32(t_seg + kHalf + hc * 32, b);
+            // rotate 16 columns of each half at a time (bounded register use)
+#pragma unroll 1
+            for (int hc = 0; hc < kHalf / 16; ++hc) {
+              uint32_t a[16], b[16];
+              tmem_ld16x2(t_seg + hc * 16, t_seg + kHalf + hc * 16, a, b);
               if (write) {
-                uint32_t o1[16], o2[16];
+                uint32_t o1[8], o2[8];
+                float b1[16], b2[16];
+                if (kBias) {
+                  load8<E>(p.bias, c0 + hc * 16, *reinterpret_cast<float(*)[8]>(&b1[0]));
+                  load8<E>(p.bias, c0 + hc * 16 + 8, *reinterpret_cast<float(*)[8]>(&b1[8]));
+                  load8<E>(p.bias, c0 + kHalf + hc * 16, *reinterpret_cast<float(*)[8]>(&b2[0]));
+                  load8<E>(p.bias, c0 + kHalf + hc * 16 + 8, *reinterpret_cast<float(*)[8]>(&b2[8]));
+                }
 #pragma unroll
-                for (int e4 = 0; e4 < 32; e4 += 4) {
-                  const int i = hc * 32 + e4;
+                for (int e4 = 0; e4 < 16; e4 += 4) {
+                  const int i = hc * 16 + e4;
                   const float4 w1 = *reinterpret_cast<const float4*>(w + i);
                   const float4 w2 = *reinterpret_cast<const float4*>(w + kHalf + i);
                   const float4 c4 = *reinterpret_cast<const float4*>(cs + i);
@@ -498,8 +659,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                     float x1 = f32(a[e4 + j]);
                     float x2 = f32(b[e4 + j]);
                     if (kBias) {
-                      x1 += ElemOps<E>::load(p.bias, c0 + i + j);
-                      x2 += ElemOps<E>::load(p.bias, c0 + kHalf + i + j);
+                      x1 += b1[e4 + j];
+                      x2 += b2[e4 + j];
                     }
                     x1 = x1 * inv * wa[j];
                     x2 = x2 * inv * wb[j];
@@ -511,8 +672,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                   o2[e4 / 2] = ElemOps<E>::pack(r2[0], r2[1]);
                   o2[e4 / 2 + 1] = ElemOps<E>::pack(r2[2], r2[3]);
                 }
-                store32(dst + hc * 32, o1);
-                store32(dst + kHalf + hc * 32, o2);
+                st16(dst + hc * 16, o1[0], o1[1], o1[2], o1[3]);
+                st16(dst + hc * 16 + 8, o1[4], o1[5], o1[6], o1[7]);
+                st16(dst + kHalf + hc * 16, o2[0], o2[1], o2[2], o2[3]);
+                st16(dst + kHalf + hc * 16 + 8, o2[4], o2[5], o2[6], o2[7]);
               }
               __syncwarp();
             }
@@ -522,7 +685,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // accumulator fully read: hand it back to the MMA warp
       tc_fence_before();
       __syncwarp();
-      if (tr != nullptr) tr[3] = global_timer_ns();
+      if (tr != nullptr) tr[5] = global_timer_ns();
       if (lane == 0) mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
       if (++acc == 2) {
         acc = 0;
@@ -534,7 +697,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
   if (trace != nullptr && threadIdx.x == 0) {
     trace[1] = global_timer_ns();
     WorkIter it = work_begin(p);
@@ -553,8 +716,15 @@ cudaError_t launch_one(int device, const CUtensorMap& tx, const CUtensorMap& tw,
   const uint64_t bit = 1ull << (device & 63);
   const size_t smem = tiled_smem_bytes();
   if (!(attr_set.load() & bit)) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    // setmaxnreg.inc waits until the CTA's register pool can grant it: the
+    // pool the kernel launches with must cover the whole split, or it would
+    // never return.  Refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (static_cast<long>(fa.numRegs) * kTiledThreads < 128L * kRegsControl + 256L * kRegsEpilogue)
+      return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }

@@ -44,11 +44,12 @@ constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kTileK = 64;     // one 128-byte swizzle row of 16-bit elements
 constexpr int kStages = 4;
-constexpr int kTiledThreads = 192;
+constexpr int kTiledThreads = 384;   // 3 warpgroups: 2 epilogue, 1 control
+constexpr int kLaunchRegs = 168;     // registers per thread at launch (65536 / 384, rounded down to 8)
 constexpr int kGroupM = 8;     // m-blocks per raster group (L2 reuse of weight tiles)
 
-constexpr int kTraceWords = 64;      // per CTA: start, end, items, then 4 words per work item
-constexpr int kTraceItems = (kTraceWords - 3) / 4;
+constexpr int kTraceWords = 64;      // per CTA: start, end, items, then 6 words per work item
+constexpr int kTraceItems = (kTraceWords - 3) / 6;
 constexpr int kMinUnitsPerCta = 8;   // k-blocks: keeps small problems from over-splitting
 
 size_t tiled_smem_bytes();

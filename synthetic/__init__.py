@@ -203,7 +203,7 @@ def make_workload(name: str, seed: Optional[int] = None, **kw) -> Workload:
     elif name == "prefill32k":
         dtype, H, L, NH, D = BF16, 4096, 5, 8, 128
         req_len = kw.get("req_len", 4096)
-        nreq = kw.get("requests", 8)
+        nreq = kw.get("requests", kw["tokens"] // req_len if "tokens" in kw else 8)
         T = nreq * req_len
         KV, q_size, eps, base, max_pos = NH * D, 4 * NH * D, 1e-6, 1e6, 4096
         slots = kw.get("pool_slots", 40000 if T <= 40000 else T + T // 5)

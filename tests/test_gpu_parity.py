@@ -121,6 +121,29 @@ def test_decode_shapes_ragged_window_all_rows():
     check_values(w, st)
 
 
+@pytest.mark.parametrize("T", [16, 64])
+def test_decode_shapes_small_token_counts(T):
+    """Small T: every column tile is split across several CTAs (up to ~4
+    contributors per tile), so the partial-tile fixup carries the result."""
+    w = workload("decode512", tokens=T)
+    st, _, flags = run_gpu(w)
+    assert flags == 0
+    check_placement(w, st)
+    check_values(w, st)
+
+
+@pytest.mark.parametrize("T", [64, 256])
+def test_many_contributors_per_split_tile(T):
+    """Few column tiles (N=512) over a long K (H=4096): every tile is cut
+    across about 8 CTAs.  At T=256 the other parts do not fit the staging
+    area and are read from the workspace; at T=64 they are staged."""
+    w = workload("tiny", tokens=T, H=4096, pool_slots=512)
+    st, _, flags = run_gpu(w)
+    assert flags == 0
+    check_placement(w, st)
+    check_values(w, st)
+
+
 def test_decode512_full():
     w = workload("decode512")
     st, _, flags = run_gpu(w)
