@@ -21,6 +21,7 @@ __all__ = [
     "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
+    "dspark_set_kernel_variant",
     "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
@@ -242,3 +243,10 @@ def dspark_write_ctx_kv_noalloc(stacked_weight, k_norm_weight, eps: float, num_l
         _ptr_array(k_pools), _ptr_array(v_pools), kstr, vstr, slots,
         None if status_flags is None else status_flags.data_ptr(), _stream_handle(stream))
     _abi.check(code, "dspark_write_ctx_kv_noalloc")
+
+
+def dspark_set_kernel_variant(bundle: Bundle, variant: str) -> None:
+    """Select the kernel of later writes: "auto" (default), "single" (one CTA
+    per 128 x 256 tile) or "pair" (CTA pairs per 256 x 256 tile)."""
+    code = {"auto": _abi.VARIANT_AUTO, "single": _abi.VARIANT_SINGLE, "pair": _abi.VARIANT_PAIR}[variant]
+    _abi.check(load().dspark_set_kernel_variant(bundle.handle, code), "dspark_set_kernel_variant")

@@ -14,7 +14,8 @@ LIB_PATH = os.path.join(PKG, "libdspark_ctx_kv.so")
 DTYPE_BF16 = 1
 DTYPE_FP16 = 2
 DTYPE_FP32 = 3
-DTYPE_OTHER = 100          # any non-bf16/fp16 weight: the pack refuses it as non-sliceable
+DTYPE_OTHER = 100
+VARIANT_AUTO, VARIANT_SINGLE, VARIANT_PAIR = 0, 1, 2          # any non-bf16/fp16 weight: the pack refuses it as non-sliceable
 MAX_LAYERS = 32
 
 FLAG_POS_RANGE = 0x1
@@ -34,7 +35,7 @@ EXPORTS = (
     "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv", "dspark_write_ctx_kv",
     "dspark_get_device_status", "dspark_clear_device_status", "dspark_bundle_get_info",
     "dspark_free_bundle", "dspark_status_string", "dspark_set_trace_buffer",
-    "dspark_write_ctx_kv_noalloc",
+    "dspark_write_ctx_kv_noalloc", "dspark_set_kernel_variant",
 )
 
 
@@ -100,6 +101,8 @@ def load() -> ctypes.CDLL:
         ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64), ctypes.POINTER(i64), i64,
         vp, vp]
     lib.dspark_write_ctx_kv_noalloc.restype = ctypes.c_int
+    lib.dspark_set_kernel_variant.argtypes = [vp, i32]
+    lib.dspark_set_kernel_variant.restype = ctypes.c_int
     lib.dspark_set_trace_buffer.argtypes = [vp, vp, i64]
     lib.dspark_set_trace_buffer.restype = ctypes.c_int
     lib.dspark_status_string.argtypes = [ctypes.c_int]

@@ -90,6 +90,8 @@ struct dspark_bundle {
   int32_t* counters;    // [sms] arrival counters, zero between launches
   int sms;              // SM count of the bundle's device
   uint64_t* trace;      // optional timeline buffer (dspark_set_trace_buffer)
+  int variant;          // DSPARK_VARIANT_* (dspark_set_kernel_variant)
+  CUtensorMap tmap_w_half;   // W_all with 128-row boxes (CTA-pair kernel)
   float eps;
   CUtensorMap tmap_w;
 };
@@ -220,7 +222,8 @@ int dspark_pack_ctx_kv(const dspark_layer_desc* layers, int32_t num_layers, int3
   }
   if (ok) ok = cudaStreamSynchronize(stream) == cudaSuccess;
   if (ok)
-    ok = make_operand_map(&b->tmap_w, b->w_all, b->dtype, hidden, b->N, b->w_pitch, kTileN);
+    ok = make_operand_map(&b->tmap_w, b->w_all, b->dtype, hidden, b->N, b->w_pitch, kTileN) &&
+         make_operand_map(&b->tmap_w_half, b->w_all, b->dtype, hidden, b->N, b->w_pitch, kTileN / 2);
   if (!ok) {
     dspark_free_bundle(b);
     return DSPARK_E_CUDA;
@@ -277,12 +280,18 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   p.NH = b->NH;
   p.D = b->D;
   p.KV = b->KV;
-  p.num_m = static_cast<int32_t>((T + kTileM - 1) / kTileM);
+  // CTA pairs (256-token tiles, tcgen05 cta_group::2) unless single-CTA tiles
+  // are asked for or the device has fewer than two SMs
+  const int pairs = b->variant != DSPARK_VARIANT_SINGLE ? pair_workers(device) : 0;
+  const bool pair = pairs > 0;
+  const int tile_rows = pair ? 2 * kTileM : kTileM;
+  p.num_m = static_cast<int32_t>((T + tile_rows - 1) / tile_rows);
   p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
   p.num_kb = (b->H + kTileK - 1) / kTileK;
   p.num_tiles = p.num_m * p.num_n;
-  int grid = 0;
-  plan_schedule(p.num_tiles, p.num_kb, b->sms, &grid, &p.dp_tiles, &p.sk_units);
+  int workers = 0;
+  plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : b->sms, &workers, &p.dp_tiles, &p.sk_units);
+  const int grid = pair ? 2 * workers : workers;
   p.workspace = b->workspace;
   p.trace = b->trace;
   p.counters = b->counters;
@@ -305,8 +314,17 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
     p.v_stride[l] = v_row_strides[l];
   }
   const cudaError_t e =
-      launch_tiled(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w, p, grid, stream);
+      pair ? launch_pair(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w_half, p, grid, stream)
+           : launch_tiled(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w, p, grid, stream);
   return e == cudaSuccess ? DSPARK_OK : DSPARK_E_CUDA;
+}
+
+int dspark_set_kernel_variant(dspark_bundle_t b, int32_t variant) {
+  if (b == nullptr) return DSPARK_E_INVALID_ARG;
+  if (variant != DSPARK_VARIANT_AUTO && variant != DSPARK_VARIANT_SINGLE && variant != DSPARK_VARIANT_PAIR)
+    return DSPARK_E_INVALID_ARG;
+  b->variant = variant;
+  return DSPARK_OK;
 }
 
 int dspark_get_device_status(dspark_bundle_t b, void* stream_, uint32_t* flags) {

@@ -61,8 +61,22 @@ struct ElemOps<__half> {
   __device__ static __forceinline__ float to_float(__half v) { return __half2float(v); }
 };
 
-constexpr uint32_t kStageBytesA = kTileM * kTileK * 2;   // 16 KB
-constexpr uint32_t kStageBytesB = kTileN * kTileK * 2;   // 32 KB
+// Operand staging of one CTA.  Single-CTA tiles are 128 tokens x 256 columns;
+// pair tiles are 256 tokens x 256 columns computed by two CTAs of a cluster
+// with tcgen05.mma.cta_group::2: each CTA holds its 128 token rows of X and
+// half (128 rows) of the W tile, so a stage is 32 KB and six fit in the ring.
+template <bool kPair>
+struct Geo {
+  static constexpr int kTileRows = kPair ? 2 * kTileM : kTileM;   // token rows of a work tile
+  static constexpr int kBRows = kPair ? kTileN / 2 : kTileN;       // W rows per CTA per stage
+  static constexpr uint32_t kStageA = kTileM * kTileK * 2;         // 16 KB
+  static constexpr uint32_t kStageB = kBRows * kTileK * 2;         // 16 KB (pair) or 32 KB
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr uint32_t kRingBytes = kStages * (kStageA + kStageB);
+};
+constexpr int kMaxStages = 6;
+constexpr uint32_t kRingBytes = Geo<false>::kRingBytes;
+static_assert(Geo<true>::kRingBytes == kRingBytes, "both layouts use the same ring");
 constexpr uint32_t kAccCols = kTileN;                    // fp32 columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;             // double buffer = 512 (all of TMEM)
 constexpr int kEpiWarps = 8;                             // two epilogue warpgroups
@@ -76,8 +90,8 @@ static_assert(128 * kRegsControl + 256 * kRegsEpilogue == 384 * kLaunchRegs,
               "the register split must use exactly the launch allocation");
 
 struct SmemBarriers {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
@@ -132,15 +146,17 @@ __device__ __forceinline__ void st16(void* dst, uint32_t a, uint32_t b, uint32_t
 // at the start of its range, which it then finishes itself: the partial tile
 // it holds in TMEM is the last to arrive.
 struct WorkIter {
-  int dp_tile;
+  int dp_tile, nw;
   int64_t start, cur;
 };
 
-__device__ __forceinline__ WorkIter work_begin(const WriteParams& p) {
+// `wid` of `nw` workers: a CTA, or a CTA pair.
+__device__ __forceinline__ WorkIter work_begin(const WriteParams& p, int wid, int nw) {
   WorkIter it;
-  it.dp_tile = blockIdx.x;
-  it.start = static_cast<int64_t>(blockIdx.x) * p.sk_units / gridDim.x;
-  it.cur = static_cast<int64_t>(blockIdx.x + 1) * p.sk_units / gridDim.x;
+  it.dp_tile = wid;
+  it.nw = nw;
+  it.start = static_cast<int64_t>(wid) * p.sk_units / nw;
+  it.cur = static_cast<int64_t>(wid + 1) * p.sk_units / nw;
   return it;
 }
 
@@ -150,7 +166,7 @@ __device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, in
     tile = it.dp_tile;
     kb0 = 0;
     kb1 = p.num_kb;
-    it.dp_tile += gridDim.x;
+    it.dp_tile += it.nw;
     return true;
   }
   if (it.cur > it.start) {
@@ -166,9 +182,9 @@ __device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, in
   return false;
 }
 
-// CTA whose stream-K range holds k-block unit u.
-__device__ __forceinline__ int sk_owner(const WriteParams& p, int64_t u) {
-  return static_cast<int>(((u + 1) * gridDim.x - 1) / p.sk_units);
+// Worker whose stream-K range holds k-block unit u.
+__device__ __forceinline__ int sk_owner(const WriteParams& p, int64_t u, int nw) {
+  return static_cast<int>(((u + 1) * nw - 1) / p.sk_units);
 }
 
 // Partial-tile slot of a CTA: [kTileN/4][kTileM] float4, so that the 32 rows
@@ -179,23 +195,31 @@ __device__ __forceinline__ float* ws_slot(const WriteParams& p, int cta, int slo
   return p.workspace + (static_cast<size_t>(cta) * 2 + slot) * kSlotFloats;
 }
 
-template <typename E, int D, bool kBias>
+template <typename E, int D, bool kBias, bool kPair>
 __global__ void __launch_bounds__(kTiledThreads, 1)
     ctx_kv_tiled_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ WriteParams p) {
+  using G = Geo<kPair>;
+  constexpr int kStages = G::kStages;
+  constexpr uint32_t kStageBytesA = G::kStageA;
+  constexpr uint32_t kStageBytesB = G::kStageB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // operand stages must sit on 1024-byte boundaries (128-byte swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* smem_a = smem;
   uint8_t* smem_b = smem + kStages * kStageBytesA;
-  SmemBarriers* bars =
-      reinterpret_cast<SmemBarriers*>(smem + kStages * (kStageBytesA + kStageBytesB));
+  SmemBarriers* bars = reinterpret_cast<SmemBarriers*>(smem + kRingBytes);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   volatile int* abort_flag = &bars->abort;
+  // a pair's two CTAs share one work sequence; rank 0 (the leader) issues MMAs
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int wid = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int nw = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -204,7 +228,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->tmem_full[b]), 1);
-      mbar_init(smem_u32(&bars->tmem_empty[b]), kEpiWarps);   // one arrival per epilogue warp
+      // one arrival per epilogue warp (of both CTAs for a pair: the leader's
+      // barrier is the one its MMA waits on)
+      mbar_init(smem_u32(&bars->tmem_empty[b]), kPair ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
@@ -215,11 +241,21 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     tma_prefetch_desc(&tmap_w);
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_u32(&bars->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (kPair) {
+    cluster_sync();   // the peer's loads and commits target this CTA's barriers
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
   uint64_t* trace = p.trace != nullptr ? p.trace + static_cast<size_t>(blockIdx.x) * kTraceWords : nullptr;
@@ -236,22 +272,38 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         uint32_t phase = 0;
         uint32_t uses[kStages] = {};
         bool ok = true;
-        WorkIter it = work_begin(p);
+        WorkIter it = work_begin(p, wid, nw);
         int tile, kb0, kb1;
         while (ok && work_next(p, it, tile, kb0, kb1)) {
           int m_blk, n_blk;
           tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+          const int a_row = m_blk * G::kTileRows + static_cast<int>(rank) * kTileM;
+          const int b_row = n_blk * kTileN + static_cast<int>(rank) * G::kBRows;
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns)) {
+            const bool got = kPair ? mbar_wait_cluster(smem_u32(&bars->empty[stage]), phase ^ 1u,
+                                                       abort_flag, p.wait_limit_ns)
+                                   : mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u,
+                                               abort_flag, p.wait_limit_ns);
+            if (!got) {
               ok = false;
               break;
             }
             const uint32_t full = smem_u32(&bars->full[stage]);
-            mbar_arrive_expect_tx(full, kStageBytesA + kStageBytesB);
-            tma_load_2d(smem_u32(smem_a + stage * kStageBytesA), &tmap_x, kb * kTileK,
-                        m_blk * kTileM, full, pol_x);
-            tma_load_2d(smem_u32(smem_b + stage * kStageBytesB), &tmap_w, kb * kTileK,
-                        n_blk * kTileN, full, pol_w);
+            if (kPair) {
+              // both CTAs' bytes complete on the leader's barrier
+              if (leader) mbar_arrive_expect_tx(full, 2 * (kStageBytesA + kStageBytesB));
+              const uint32_t full_leader = mapa_shared(full, 0);
+              tma_load_2d_pair(smem_u32(smem_a + stage * kStageBytesA), &tmap_x, kb * kTileK, a_row,
+                               full_leader, pol_x);
+              tma_load_2d_pair(smem_u32(smem_b + stage * kStageBytesB), &tmap_w, kb * kTileK, b_row,
+                               full_leader, pol_w);
+            } else {
+              mbar_arrive_expect_tx(full, kStageBytesA + kStageBytesB);
+              tma_load_2d(smem_u32(smem_a + stage * kStageBytesA), &tmap_x, kb * kTileK, a_row, full,
+                          pol_x);
+              tma_load_2d(smem_u32(smem_b + stage * kStageBytesB), &tmap_w, kb * kTileK, b_row, full,
+                          pol_w);
+            }
             ++uses[stage];
             if (++stage == kStages) {
               stage = 0;
@@ -264,34 +316,42 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           flag(p, DSPARK_FLAG_TIMEOUT);
         }
         // every load issued must land before the CTA may exit (bounded by time
-        // only: an abort must not cut this wait short)
+        // only: an abort must not cut this wait short).  A pair's peer sees its
+        // loads land only through the leader's MMA releasing the stage.
         int never = 0;
 #pragma unroll
-        for (int s = 0; s < kStages; ++s)
-          if (uses[s] > 0) mbar_wait(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
+        for (int s = 0; s < kStages; ++s) {
+          if (uses[s] == 0) continue;
+          if (!kPair)
+            mbar_wait(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
+          else if (leader)
+            mbar_wait_cluster(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
+          else
+            mbar_wait_cluster(smem_u32(&bars->empty[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
+        }
       }
     } else if (warp == kMmaWarp) {
       // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idesc = f16_instr_desc(ElemOps<E>::kFmt, kTileM, kTileN);
+      if (lane == 0 && leader) {
+        constexpr uint32_t idesc = f16_instr_desc(ElemOps<E>::kFmt, G::kTileRows, kTileN);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
         bool issued = false;
-        WorkIter it = work_begin(p);
+        WorkIter it = work_begin(p, wid, nw);
         int tile, kb0, kb1;
         while (ok && work_next(p, it, tile, kb0, kb1)) {
-          if (!mbar_wait(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort_flag,
-                         p.wait_limit_ns)) {
+          if (!mbar_wait_cluster(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort_flag,
+                                 p.wait_limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kAccCols;
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(smem_u32(&bars->full[stage]), phase, abort_flag, p.wait_limit_ns)) {
+            if (!mbar_wait_cluster(smem_u32(&bars->full[stage]), phase, abort_flag, p.wait_limit_ns)) {
               ok = false;
               break;
             }
@@ -301,18 +361,28 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
 #pragma unroll
             for (int k = 0; k < kTileK / 16; ++k) {
               // advancing 16 elements along K = 32 bytes inside the swizzle atom
-              umma_f16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
-                       idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+              const uint64_t ad = sw128_kmajor_desc(a0 + k * 32), bd = sw128_kmajor_desc(b0 + k * 32);
+              const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+              if (kPair)
+                umma_f16_pair(d_tmem, ad, bd, idesc, accum);
+              else
+                umma_f16(d_tmem, ad, bd, idesc, accum);
             }
             issued = true;
-            umma_commit(smem_u32(&bars->empty[stage]));
+            if (kPair)
+              umma_commit_pair(smem_u32(&bars->empty[stage]), 0x3);
+            else
+              umma_commit(smem_u32(&bars->empty[stage]));
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit(smem_u32(&bars->tmem_full[acc]));
+          if (kPair)
+            umma_commit_pair(smem_u32(&bars->tmem_full[acc]), 0x3);
+          else
+            umma_commit(smem_u32(&bars->tmem_full[acc]));
           if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
@@ -324,7 +394,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         }
         if (issued) {
           // all MMAs issued by this thread complete before TMEM is released
-          umma_commit(smem_u32(&bars->drain));
+          if (kPair)
+            umma_commit_pair(smem_u32(&bars->drain), 0x1);
+          else
+            umma_commit(smem_u32(&bars->drain));
           int never = 0;
           mbar_wait(smem_u32(&bars->drain), 0, &never, p.wait_limit_ns);
         }
@@ -344,7 +417,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int item = 0;
-    WorkIter it = work_begin(p);
+    WorkIter it = work_begin(p, wid, nw);
     int tile, kb0, kb1;
     while (work_next(p, it, tile, kb0, kb1)) {
       int m_blk, n_blk;
@@ -357,7 +430,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       }
       // ---- per-token decision (same for every head of the tile); it does not
       // depend on the accumulator, so it runs while the MMAs are in flight
-      const int64_t t = static_cast<int64_t>(m_blk) * kTileM + row;
+      const int64_t row0 = static_cast<int64_t>(m_blk) * G::kTileRows + static_cast<int64_t>(rank) * kTileM;
+      const int64_t t = row0 + row;
       bool write = false;
       int64_t loc = 0, pos = 0;
       if (t < p.T) {
@@ -384,8 +458,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         for (int b = group * 128; b < D * 4; b += 256) prefetch_l2(cs_row + b);
       }
       // the outcome must be warp-uniform: tcgen05.ld below is .sync.aligned
-      const bool got = mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort_flag,
-                                 p.wait_limit_ns);
+      const bool got = mbar_wait_cluster(smem_u32(&bars->tmem_full[acc]), acc_phase, abort_flag,
+                                         p.wait_limit_ns);
       // stamps come from the thread of row 0 of the first group
       uint64_t* tr =
           (trace != nullptr && etid == 0 && item < kTraceItems) ? trace + 3 + 6 * item : nullptr;
@@ -413,9 +487,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       bool finish = true;
       if (kb0 != 0 || kb1 != p.num_kb) {
         const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
-        const int c_first = sk_owner(p, u0);
-        const int c_last = sk_owner(p, u0 + p.num_kb - 1);
-        const int me = static_cast<int>(blockIdx.x);
+        // contributors are workers (CTAs, or CTA pairs whose halves are
+        // finished independently: the slot and counter of a pair CTA carry its rank)
+        const int c_first = sk_owner(p, u0, nw);
+        const int c_last = sk_owner(p, u0 + p.num_kb - 1, nw);
+        const int me = wid;
+        auto cta_of = [&](int c) { return kPair ? 2 * c + static_cast<int>(rank) : c; };
+        int32_t* counter = p.counters + cta_of(c_last);
         // If every other contributor has already published (the usual case for
         // a CTA's last work item), this CTA finishes the tile without
         // publishing its own part.  An earlier item of a CTA is almost never
@@ -423,9 +501,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         finish = false;
         if (final_item) {
           if (etid == 0) {
-            const int seen = ld_acquire_gpu(p.counters + c_last);
+            const int seen = ld_acquire_gpu(counter);
             const int done = seen == c_last - c_first;
-            if (done) p.counters[c_last] = 0;   // no other contributor touches it again
+            if (done) *counter = 0;   // no other contributor touches it again
             *reinterpret_cast<volatile int*>(&bars->last_arrival) = done;
           }
           named_barrier(1, kEpiThreads);
@@ -433,7 +511,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           named_barrier(1, kEpiThreads);
         }
         if (!finish) {
-          float4* mine = reinterpret_cast<float4*>(ws_slot(p, me, kb0 > 0 ? 0 : 1));
+          float4* mine = reinterpret_cast<float4*>(ws_slot(p, cta_of(me), kb0 > 0 ? 0 : 1));
 #pragma unroll 1
           for (int ch = ch_lo; ch < ch_hi; ch += 2) {
             uint32_t v[32], u[32];
@@ -454,9 +532,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           named_barrier(1, kEpiThreads);
           if (tr != nullptr) tr[4] = global_timer_ns();   // dump visible
           if (etid == 0) {
-            const int old = atomicAdd(p.counters + c_last, 1);
+            const int old = atomicAdd(counter, 1);
             const int last = old == c_last - c_first;
-            if (last) p.counters[c_last] = 0;   // ready for the next launch
+            if (last) *counter = 0;   // ready for the next launch
             __threadfence();
             *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
           }
@@ -473,14 +551,14 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           // CTA's own part taken from TMEM at its place), so the result does not
           // depend on which contributor arrived last.  Each group sums its half
           // of the columns.
-          const int64_t rows_left = static_cast<int64_t>(p.T) - static_cast<int64_t>(m_blk) * kTileM;
-          const int rv = rows_left < kTileM ? static_cast<int>(rows_left) : kTileM;
+          const int64_t rows_left = static_cast<int64_t>(p.T) - row0;
+          const int rv = rows_left <= 0 ? 0 : (rows_left < kTileM ? static_cast<int>(rows_left) : kTileM);
           const int n_oth = c_last - c_first;
           // After the CTA's last MMA the operand ring is idle: the other parts
           // are staged there (each group in its own half) with many asynchronous
           // 16-byte copies in flight; each thread copies, then reads, only its
           // own row.  Otherwise they are read from the workspace directly.
-          constexpr int kHalfRingF4 = kStages * (kStageBytesA + kStageBytesB) / 32;
+          constexpr int kHalfRingF4 = kRingBytes / 32;
           const int per_chunk = n_oth * 8 * rv;           // float4 per column chunk
           const bool staged = final_item && per_chunk <= kHalfRingF4;
           int cpr = kChunks / 2;
@@ -498,7 +576,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
               for (int c = c_first; c <= c_last; ++c) {
                 if (c == me) continue;
                 const float4* src =
-                    reinterpret_cast<const float4*>(ws_slot(p, c, c == c_first ? 1 : 0));
+                    reinterpret_cast<const float4*>(ws_slot(p, cta_of(c), c == c_first ? 1 : 0));
                 for (int cl = 0; cl < nch; ++cl)
 #pragma unroll
                   for (int j = 0; j < 8; ++j)
@@ -522,7 +600,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                   if (row < rv) {
                     const float4* src =
                         staged ? ring_f4 + (oi * nch + cl) * 8 * rv + row
-                               : reinterpret_cast<const float4*>(ws_slot(p, c, c == c_first ? 1 : 0)) +
+                               : reinterpret_cast<const float4*>(ws_slot(p, cta_of(c), c == c_first ? 1 : 0)) +
                                      ch * 8 * kTileM + row;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -686,7 +764,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (tr != nullptr) tr[5] = global_timer_ns();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
+      if (lane == 0) {
+        if (kPair)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&bars->tmem_empty[acc]), 0));
+        else
+          mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -695,22 +778,32 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (kPair) {
+    cluster_sync();   // the leader's MMAs read the peer's operands until here
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == kMmaWarp) {
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
+  }
   if (trace != nullptr && threadIdx.x == 0) {
     trace[1] = global_timer_ns();
-    WorkIter it = work_begin(p);
+    WorkIter it = work_begin(p, wid, nw);
     int tile, kb0, kb1, n = 0;
     while (work_next(p, it, tile, kb0, kb1)) ++n;
     trace[2] = static_cast<uint64_t>(n);
   }
 }
 
-template <typename E, int D, bool kBias>
+template <typename E, int D, bool kBias, bool kPair>
 cudaError_t launch_one(int device, const CUtensorMap& tx, const CUtensorMap& tw,
                        const WriteParams& p, int grid, cudaStream_t stream) {
-  auto kern = ctx_kv_tiled_kernel<E, D, kBias>;
+  auto kern = ctx_kv_tiled_kernel<E, D, kBias, kPair>;
   // the opt-in shared-memory size is set once per device and instantiation
   static std::atomic<uint64_t> attr_set{0};
   const uint64_t bit = 1ull << (device & 63);
@@ -728,31 +821,87 @@ cudaError_t launch_one(int device, const CUtensorMap& tx, const CUtensorMap& tw,
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
-  kern<<<grid, kTiledThreads, smem, stream>>>(tx, tw, p);
-  return cudaGetLastError();
+  if (!kPair) {
+    kern<<<grid, kTiledThreads, smem, stream>>>(tx, tw, p);
+    return cudaGetLastError();
+  }
+  // CTA pairs: clusters of two along x
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kTiledThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tx, tw, p);
+}
+
+template <bool kPair>
+cudaError_t dispatch(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tx,
+                     const CUtensorMap& tw, const WriteParams& p, int grid, cudaStream_t stream) {
+  if (dtype == DSPARK_DTYPE_BF16) {
+    if (head_dim == 128)
+      return has_bias ? launch_one<__nv_bfloat16, 128, true, kPair>(device, tx, tw, p, grid, stream)
+                      : launch_one<__nv_bfloat16, 128, false, kPair>(device, tx, tw, p, grid, stream);
+    return has_bias ? launch_one<__nv_bfloat16, 64, true, kPair>(device, tx, tw, p, grid, stream)
+                    : launch_one<__nv_bfloat16, 64, false, kPair>(device, tx, tw, p, grid, stream);
+  }
+  if (head_dim == 128)
+    return has_bias ? launch_one<__half, 128, true, kPair>(device, tx, tw, p, grid, stream)
+                    : launch_one<__half, 128, false, kPair>(device, tx, tw, p, grid, stream);
+  return has_bias ? launch_one<__half, 64, true, kPair>(device, tx, tw, p, grid, stream)
+                  : launch_one<__half, 64, false, kPair>(device, tx, tw, p, grid, stream);
 }
 
 }  // namespace
 
 size_t tiled_smem_bytes() {
-  return 1024 /* alignment slack */ + kStages * (kStageBytesA + kStageBytesB) + sizeof(SmemBarriers);
+  return 1024 /* alignment slack */ + kRingBytes + sizeof(SmemBarriers);
 }
 
 cudaError_t launch_tiled(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tx,
                          const CUtensorMap& tw, const WriteParams& p, int grid,
                          cudaStream_t stream) {
-  if (dtype == DSPARK_DTYPE_BF16) {
-    if (head_dim == 128)
-      return has_bias ? launch_one<__nv_bfloat16, 128, true>(device, tx, tw, p, grid, stream)
-                      : launch_one<__nv_bfloat16, 128, false>(device, tx, tw, p, grid, stream);
-    return has_bias ? launch_one<__nv_bfloat16, 64, true>(device, tx, tw, p, grid, stream)
-                    : launch_one<__nv_bfloat16, 64, false>(device, tx, tw, p, grid, stream);
-  }
-  if (head_dim == 128)
-    return has_bias ? launch_one<__half, 128, true>(device, tx, tw, p, grid, stream)
-                    : launch_one<__half, 128, false>(device, tx, tw, p, grid, stream);
-  return has_bias ? launch_one<__half, 64, true>(device, tx, tw, p, grid, stream)
-                  : launch_one<__half, 64, false>(device, tx, tw, p, grid, stream);
+  return dispatch<false>(device, dtype, head_dim, has_bias, tx, tw, p, grid, stream);
+}
+
+cudaError_t launch_pair(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tx,
+                        const CUtensorMap& tw_half, const WriteParams& p, int grid,
+                        cudaStream_t stream) {
+  return dispatch<true>(device, dtype, head_dim, has_bias, tx, tw_half, p, grid, stream);
+}
+
+int pair_workers(int device) {
+  // every instantiation has the same block size, shared memory and registers,
+  // so one of them answers for all
+  static std::atomic<int> cache[64];
+  const int d = device & 63;
+  int n = cache[d].load();
+  if (n > 0) return n;
+  auto kern = ctx_kv_tiled_kernel<__nv_bfloat16, 128, false, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(tiled_smem_bytes())) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kTiledThreads, 1, 1);
+  cfg.dynamicSmemBytes = tiled_smem_bytes();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return 0;
+  cache[d].store(clusters);
+  return clusters;
 }
 
 }  // namespace dspark

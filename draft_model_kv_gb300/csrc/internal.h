@@ -43,7 +43,6 @@ struct WriteParams {
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kTileK = 64;     // one 128-byte swizzle row of 16-bit elements
-constexpr int kStages = 4;
 constexpr int kTiledThreads = 384;   // 3 warpgroups: 2 epilogue, 1 control
 constexpr int kLaunchRegs = 168;     // registers per thread at launch (65536 / 384, rounded down to 8)
 constexpr int kGroupM = 8;     // m-blocks per raster group (L2 reuse of weight tiles)
@@ -76,11 +75,21 @@ inline void plan_schedule(int tiles, int num_kb, int sms, int* grid, int* dp_til
   }
 }
 
-// Launch the tiled kernel for the bundle dtype (1 = bf16, 2 = fp16).  Returns
-// the CUDA error of the launch.
+// Launch the fused kernel for the bundle dtype (1 = bf16, 2 = fp16).  Returns
+// the CUDA error of the launch.  launch_tiled: one CTA per 128 x 256 tile
+// (grid = CTAs, num_m counts 128-token blocks, tmap_w box 256 rows);
+// launch_pair: CTA pairs per 256 x 256 tile (grid = 2 x pairs, num_m counts
+// 256-token blocks, tmap_w box 128 rows), the schedule planned over pairs.
 cudaError_t launch_tiled(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tmap_x,
                          const CUtensorMap& tmap_w, const WriteParams& p, int grid,
                          cudaStream_t stream);
+
+cudaError_t launch_pair(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tmap_x,
+                        const CUtensorMap& tmap_w_half, const WriteParams& p, int grid,
+                        cudaStream_t stream);
+
+// Number of CTA pairs that can be resident at once on `device` (0 if unknown).
+int pair_workers(int device);
 
 // Convert a [n] bf16 / fp16 / fp32 vector to fp32 (bundle packing).
 cudaError_t launch_to_fp32(const void* src, int dtype, float* dst, int n, cudaStream_t stream);

@@ -39,7 +39,7 @@ def tol(w):
     return (2e-2, 2e-2) if w.dtype == "bf16" else (5e-3, 5e-3)
 
 
-def run_gpu(w, row_pad=0, hidden_pad=0, st=None):
+def run_gpu(w, row_pad=0, hidden_pad=0, st=None, variant="auto"):
     import draft_model_kv_gb300 as dk
     st = st or stage(w, row_pad=row_pad)
     x = st["ctx_hidden"]
@@ -48,6 +48,7 @@ def run_gpu(w, row_pad=0, hidden_pad=0, st=None):
         wide[:, :w.H] = x
         x = wide[:, :w.H]
     b = dk.dspark_pack_ctx_kv(st["layers"], w.H)
+    dk.dspark_set_kernel_variant(b, variant)
     dk.dspark_clear_device_status(b)
     dk.dspark_write_ctx_kv(b, x, st["positions"], st["cos_sin"], st["cache_loc"], st["k_pools"],
                            st["v_pools"], commit_lens=st["commit_lens"],
@@ -94,51 +95,59 @@ def edge_sample(T, n_random=192, seed=0):
 
 # ------------------------------------------------------------------ small cases, all rows
 
-def test_tiny_full():
+VARIANTS = ["single", "pair"]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_tiny_full(variant):
     w = workload("tiny")
-    st, _, flags = run_gpu(w)
+    st, _, flags = run_gpu(w, variant=variant)
     assert flags == 0
     check_placement(w, st)
     check_values(w, st)
 
 
-@pytest.mark.parametrize("T", [1, 7, 127, 128, 129, 300])
-def test_tiny_ragged_token_counts(T):
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("T", [1, 7, 127, 128, 129, 255, 256, 257, 300])
+def test_tiny_ragged_token_counts(T, variant):
     w = workload("tiny", tokens=T)
-    st, _, flags = run_gpu(w)
+    st, _, flags = run_gpu(w, variant=variant)
     assert flags == 0
     check_placement(w, st)
     check_values(w, st)
 
 
-def test_decode_shapes_ragged_window_all_rows():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_decode_shapes_ragged_window_all_rows(variant):
     """Qwen3-8B-shaped decode (H=4096, 5 layers, 8x128) with 37 windows of 8:
-    3 token tiles with a ragged tail, 40 column tiles, commit_lens truncation."""
+    token tiles with a ragged tail, 40 column tiles, commit_lens truncation."""
     w = workload("decode512", tokens=296)
-    st, _, flags = run_gpu(w)
+    st, _, flags = run_gpu(w, variant=variant)
     assert flags == 0
     check_placement(w, st)
     check_values(w, st)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("T", [16, 64])
-def test_decode_shapes_small_token_counts(T):
+def test_decode_shapes_small_token_counts(T, variant):
     """Small T: every column tile is split across several CTAs (up to ~4
     contributors per tile), so the partial-tile fixup carries the result."""
     w = workload("decode512", tokens=T)
-    st, _, flags = run_gpu(w)
+    st, _, flags = run_gpu(w, variant=variant)
     assert flags == 0
     check_placement(w, st)
     check_values(w, st)
 
 
-@pytest.mark.parametrize("T", [64, 256])
-def test_many_contributors_per_split_tile(T):
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("T", [64, 256, 512])
+def test_many_contributors_per_split_tile(T, variant):
     """Few column tiles (N=512) over a long K (H=4096): every tile is cut
     across about 8 CTAs.  At T=256 the other parts do not fit the staging
     area and are read from the workspace; at T=64 they are staged."""
     w = workload("tiny", tokens=T, H=4096, pool_slots=512)
-    st, _, flags = run_gpu(w)
+    st, _, flags = run_gpu(w, variant=variant)
     assert flags == 0
     check_placement(w, st)
     check_values(w, st)
@@ -237,10 +246,11 @@ def test_out_of_range_position_and_loc_are_flagged_and_skipped():
     assert dk.dspark_get_device_status(b) == 0
 
 
-def test_repeat_is_bitwise_deterministic():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_repeat_is_bitwise_deterministic(variant):
     w = workload("decode512", tokens=128)
-    st1, _, _ = run_gpu(w)
-    st2, _, _ = run_gpu(w)
+    st1, _, _ = run_gpu(w, variant=variant)
+    st2, _, _ = run_gpu(w, variant=variant)
     for a, b in zip(st1["k_pools"] + st1["v_pools"], st2["k_pools"] + st2["v_pools"]):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
