@@ -342,7 +342,9 @@ def run_gpu(args, w):
 
 NCU_TRAFFIC = {
     # per-launch DRAM bytes (read + write) of the fused kernel from one ncu
-    # capture; null until a capture of the current kernel exists
+    # capture of the current kernel (profiles/ctx_kv_kernel_decode512.md);
+    # workloads without a capture report null
+    "decode512": 91.918080e6 + 10.501120e6,
 }
 
 
