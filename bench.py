@@ -308,7 +308,7 @@ def run_gpu(args, w):
     achieved_tf = flops / (mean_ms * 1e-3) / 1e12
     achieved_gb = bytes_ / (mean_ms * 1e-3) / 1e9
     bound = "tensor" if t_tc >= t_hbm else "hbm"
-    traffic = ncu_traffic(w.name)
+    traffic = ncu_traffic(w.name, w.T)
     roof_tc = {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16_tflops"],
                "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16_tflops"], "traffic": traffic,
                "peak_source": pk["source"] + " (burst: the kernel is timed alone)"}
@@ -341,15 +341,14 @@ def run_gpu(args, w):
 
 
 NCU_TRAFFIC = {
-    # per-launch DRAM bytes (read + write) of the fused kernel from one ncu
-    # capture of the current kernel (profiles/ctx_kv_kernel_decode512.md);
-    # workloads without a capture report null
-    "decode512": 91.918080e6 + 10.501120e6,
+    # (workload, tokens) -> per-launch DRAM bytes (read + write) of the fused
+    # kernel from one ncu capture of the kernel as it stands (summaries under
+    # profiles/); anything without a capture of the current kernel reports null
 }
 
 
-def ncu_traffic(name):
-    return NCU_TRAFFIC.get(name)
+def ncu_traffic(name, tokens):
+    return NCU_TRAFFIC.get((name, tokens))
 
 
 def make(args):

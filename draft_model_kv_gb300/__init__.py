@@ -247,6 +247,8 @@ def dspark_write_ctx_kv_noalloc(stacked_weight, k_norm_weight, eps: float, num_l
 
 def dspark_set_kernel_variant(bundle: Bundle, variant: str) -> None:
     """Select the kernel of later writes: "auto" (default), "single" (one CTA
-    per 128 x 256 tile) or "pair" (CTA pairs per 256 x 256 tile)."""
-    code = {"auto": _abi.VARIANT_AUTO, "single": _abi.VARIANT_SINGLE, "pair": _abi.VARIANT_PAIR}[variant]
+    per 128 x 256 tile), "pair" (CTA pairs per 256 x 256 tile) or "stream"
+    (weight streaming, at most 256 tokens)."""
+    code = {"auto": _abi.VARIANT_AUTO, "single": _abi.VARIANT_SINGLE, "pair": _abi.VARIANT_PAIR,
+            "stream": _abi.VARIANT_STREAM}[variant]
     _abi.check(load().dspark_set_kernel_variant(bundle.handle, code), "dspark_set_kernel_variant")

@@ -15,7 +15,7 @@ DTYPE_BF16 = 1
 DTYPE_FP16 = 2
 DTYPE_FP32 = 3
 DTYPE_OTHER = 100
-VARIANT_AUTO, VARIANT_SINGLE, VARIANT_PAIR = 0, 1, 2          # any non-bf16/fp16 weight: the pack refuses it as non-sliceable
+VARIANT_AUTO, VARIANT_SINGLE, VARIANT_PAIR, VARIANT_STREAM = 0, 1, 2, 3          # any non-bf16/fp16 weight: the pack refuses it as non-sliceable
 MAX_LAYERS = 32
 
 FLAG_POS_RANGE = 0x1

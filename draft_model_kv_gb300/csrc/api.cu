@@ -267,10 +267,6 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   if (cudaGetDevice(&device) != cudaSuccess || device != b->device) return DSPARK_E_DEVICE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
 
-  CUtensorMap tmap_x;
-  if (!make_operand_map(&tmap_x, ctx_hidden, b->dtype, b->H, T, hidden_row_stride, kTileM))
-    return DSPARK_E_CUDA;
-
   WriteParams p;
   std::memset(&p, 0, sizeof(p));
   p.T = static_cast<int32_t>(T);
@@ -280,21 +276,7 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   p.NH = b->NH;
   p.D = b->D;
   p.KV = b->KV;
-  // CTA pairs (256-token tiles, tcgen05 cta_group::2) unless single-CTA tiles
-  // are asked for or the device has fewer than two SMs
-  const int pairs = b->variant != DSPARK_VARIANT_SINGLE ? pair_workers(device) : 0;
-  const bool pair = pairs > 0;
-  const int tile_rows = pair ? 2 * kTileM : kTileM;
-  p.num_m = static_cast<int32_t>((T + tile_rows - 1) / tile_rows);
-  p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
   p.num_kb = (b->H + kTileK - 1) / kTileK;
-  p.num_tiles = p.num_m * p.num_n;
-  int workers = 0;
-  plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : b->sms, &workers, &p.dp_tiles, &p.sk_units);
-  const int grid = pair ? 2 * workers : workers;
-  p.workspace = b->workspace;
-  p.trace = b->trace;
-  p.counters = b->counters;
   p.positions = positions;
   p.cache_loc = cache_loc;
   p.commit_lens = commit_lens;
@@ -306,6 +288,9 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   p.bias = b->bias;
   p.eps = b->eps;
   p.status = b->status;
+  p.workspace = b->workspace;
+  p.counters = b->counters;
+  p.trace = b->trace;
   p.wait_limit_ns = 2000000000ull;
   for (int l = 0; l < b->L; ++l) {
     p.k_pool[l] = k_pools[l];
@@ -313,6 +298,44 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
     p.k_stride[l] = k_row_strides[l];
     p.v_stride[l] = v_row_strides[l];
   }
+
+  // Small token counts: stream the weights (weights as the MMA's M side).
+  int t_pad = 0, stages = 0;
+  uint32_t stage_b = 0, acc_stride = 0, tmem_cols = 0;
+  const bool stream_ok = b->KV % 128 == 0 &&
+                         stream_plan(T, &t_pad, &stages, &stage_b, &acc_stride, &tmem_cols);
+  const bool use_stream = stream_ok && (b->variant == DSPARK_VARIANT_STREAM ||
+                                        (b->variant == DSPARK_VARIANT_AUTO && T <= kStreamAutoMaxTokens));
+  if (b->variant == DSPARK_VARIANT_STREAM && !stream_ok) return DSPARK_E_INVALID_ARG;
+  if (use_stream) {
+    CUtensorMap tmap_x;
+    if (!make_operand_map(&tmap_x, ctx_hidden, b->dtype, b->H, T, hidden_row_stride,
+                          static_cast<uint32_t>(t_pad)))
+      return DSPARK_E_CUDA;
+    p.num_m = 1;
+    p.num_n = static_cast<int32_t>(b->N / 128);
+    p.num_tiles = p.num_n;
+    int grid = 0;
+    plan_schedule(p.num_tiles, p.num_kb, b->sms, &grid, &p.dp_tiles, &p.sk_units);
+    const cudaError_t e = launch_stream(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w_half, p,
+                                        t_pad, stages, stage_b, acc_stride, tmem_cols, grid, stream);
+    return e == cudaSuccess ? DSPARK_OK : DSPARK_E_CUDA;
+  }
+
+  CUtensorMap tmap_x;
+  if (!make_operand_map(&tmap_x, ctx_hidden, b->dtype, b->H, T, hidden_row_stride, kTileM))
+    return DSPARK_E_CUDA;
+  // CTA pairs (256-token tiles, tcgen05 cta_group::2) unless single-CTA tiles
+  // are asked for or the device has fewer than two SMs
+  const int pairs = b->variant != DSPARK_VARIANT_SINGLE ? pair_workers(device) : 0;
+  const bool pair = pairs > 0;
+  const int tile_rows = pair ? 2 * kTileM : kTileM;
+  p.num_m = static_cast<int32_t>((T + tile_rows - 1) / tile_rows);
+  p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
+  p.num_tiles = p.num_m * p.num_n;
+  int workers = 0;
+  plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : b->sms, &workers, &p.dp_tiles, &p.sk_units);
+  const int grid = pair ? 2 * workers : workers;
   const cudaError_t e =
       pair ? launch_pair(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w_half, p, grid, stream)
            : launch_tiled(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w, p, grid, stream);
@@ -321,7 +344,8 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
 
 int dspark_set_kernel_variant(dspark_bundle_t b, int32_t variant) {
   if (b == nullptr) return DSPARK_E_INVALID_ARG;
-  if (variant != DSPARK_VARIANT_AUTO && variant != DSPARK_VARIANT_SINGLE && variant != DSPARK_VARIANT_PAIR)
+  if (variant != DSPARK_VARIANT_AUTO && variant != DSPARK_VARIANT_SINGLE && variant != DSPARK_VARIANT_PAIR &&
+      variant != DSPARK_VARIANT_STREAM)
     return DSPARK_E_INVALID_ARG;
   b->variant = variant;
   return DSPARK_OK;

@@ -27,39 +27,11 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace dspark {
 namespace {
-
-template <typename E>
-struct ElemOps;
-
-template <>
-struct ElemOps<__nv_bfloat16> {
-  static constexpr uint32_t kFmt = 1;
-  __device__ static __forceinline__ uint32_t pack(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __device__ static __forceinline__ float load(const void* p, int64_t i) {
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
-  }
-  __device__ static __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
-};
-
-template <>
-struct ElemOps<__half> {
-  static constexpr uint32_t kFmt = 0;
-  __device__ static __forceinline__ uint32_t pack(float a, float b) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __device__ static __forceinline__ float load(const void* p, int64_t i) {
-    return __half2float(reinterpret_cast<const __half*>(p)[i]);
-  }
-  __device__ static __forceinline__ float to_float(__half v) { return __half2float(v); }
-};
 
 // Operand staging of one CTA.  Single-CTA tiles are 128 tokens x 256 columns;
 // pair tiles are 256 tokens x 256 columns computed by two CTAs of a cluster
@@ -109,90 +81,6 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   const int r = tile - group * group_size;
   m_blk = first_m + r % gm;
   n_blk = r / gm;
-}
-
-__device__ __forceinline__ void flag(const WriteParams& p, uint32_t bits) {
-  atomicOr(p.status, bits);
-}
-
-__device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
-
-// 8 consecutive 16-bit values (one 16-byte load) widened to fp32.
-template <typename E>
-__device__ __forceinline__ void load8(const void* base, int64_t idx, float (&out)[8]) {
-  const uint4 q = *reinterpret_cast<const uint4*>(reinterpret_cast<const E*>(base) + idx);
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFFu), hi = static_cast<uint16_t>(w[i] >> 16);
-    E a, b;
-    memcpy(&a, &lo, 2);
-    memcpy(&b, &hi, 2);
-    out[2 * i] = ElemOps<E>::to_float(a);
-    out[2 * i + 1] = ElemOps<E>::to_float(b);
-  }
-}
-
-// 16-byte store of 8 packed 16-bit outputs.
-__device__ __forceinline__ void st16(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
-}
-
-// Work of one CTA: first its whole tiles of the data-parallel waves, then its
-// contiguous range of the stream-K k-block space, walked from its end back to
-// its start.  The backward walk makes a CTA begin with the (usually small)
-// first k-blocks of the tile at the end of its range, publish that part while
-// it computes the rest, and end with the (usually large) last part of the tile
-// at the start of its range, which it then finishes itself: the partial tile
-// it holds in TMEM is the last to arrive.
-struct WorkIter {
-  int dp_tile, nw;
-  int64_t start, cur;
-};
-
-// `wid` of `nw` workers: a CTA, or a CTA pair.
-__device__ __forceinline__ WorkIter work_begin(const WriteParams& p, int wid, int nw) {
-  WorkIter it;
-  it.dp_tile = wid;
-  it.nw = nw;
-  it.start = static_cast<int64_t>(wid) * p.sk_units / nw;
-  it.cur = static_cast<int64_t>(wid + 1) * p.sk_units / nw;
-  return it;
-}
-
-__device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, int& tile, int& kb0,
-                                          int& kb1) {
-  if (it.dp_tile < p.dp_tiles) {
-    tile = it.dp_tile;
-    kb0 = 0;
-    kb1 = p.num_kb;
-    it.dp_tile += it.nw;
-    return true;
-  }
-  if (it.cur > it.start) {
-    const int64_t t = (it.cur - 1) / p.num_kb;
-    const int64_t tile_start = t * p.num_kb;
-    const int64_t lo = it.start > tile_start ? it.start : tile_start;
-    kb0 = static_cast<int>(lo - tile_start);
-    kb1 = static_cast<int>(it.cur - tile_start);
-    it.cur = lo;
-    tile = p.dp_tiles + static_cast<int>(t);
-    return true;
-  }
-  return false;
-}
-
-// Worker whose stream-K range holds k-block unit u.
-__device__ __forceinline__ int sk_owner(const WriteParams& p, int64_t u, int nw) {
-  return static_cast<int>(((u + 1) * nw - 1) / p.sk_units);
-}
-
-// Partial-tile slot of a CTA: [kTileN/4][kTileM] float4, so that the 32 rows
-// of a warp write one contiguous 512-byte run per 4 columns.
-constexpr int kSlotFloats = kTileM * kTileN;
-
-__device__ __forceinline__ float* ws_slot(const WriteParams& p, int cta, int slot) {
-  return p.workspace + (static_cast<size_t>(cta) * 2 + slot) * kSlotFloats;
 }
 
 template <typename E, int D, bool kBias, bool kPair>
@@ -457,6 +345,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         const char* cs_row = reinterpret_cast<const char*>(p.cos_sin + pos * D);
         for (int b = group * 128; b < D * 4; b += 256) prefetch_l2(cs_row + b);
       }
+      // A CTA's last item is normally the last part of its split tile to be
+      // computed: check now, while its MMAs run, whether the other parts are
+      // already published (the decision is read after the barrier below).
+      const bool cut = kb0 != 0 || kb1 != p.num_kb;
+      if (cut && final_item && etid == 0) {
+        const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
+        const int cf = sk_owner(p, u0, nw), cl = sk_owner(p, u0 + p.num_kb - 1, nw);
+        const int seen = ld_acquire_gpu(p.counters + (kPair ? 2 * cl + static_cast<int>(rank) : cl));
+        *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == cl - cf;
+      }
       // the outcome must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = mbar_wait_cluster(smem_u32(&bars->tmem_full[acc]), acc_phase, abort_flag,
                                          p.wait_limit_ns);
@@ -485,7 +383,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // ---- a tile cut between CTAs: publish this part; the last contributor
       // to arrive adds the other parts into its accumulator and finishes it
       bool finish = true;
-      if (kb0 != 0 || kb1 != p.num_kb) {
+      if (cut) {
         const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
         // contributors are workers (CTAs, or CTA pairs whose halves are
         // finished independently: the slot and counter of a pair CTA carry its rank)
@@ -494,22 +392,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         const int me = wid;
         auto cta_of = [&](int c) { return kPair ? 2 * c + static_cast<int>(rank) : c; };
         int32_t* counter = p.counters + cta_of(c_last);
-        // If every other contributor has already published (the usual case for
-        // a CTA's last work item), this CTA finishes the tile without
-        // publishing its own part.  An earlier item of a CTA is almost never
-        // the last to arrive, so it skips the check.
-        finish = false;
-        if (final_item) {
-          if (etid == 0) {
-            const int seen = ld_acquire_gpu(counter);
-            const int done = seen == c_last - c_first;
-            if (done) *counter = 0;   // no other contributor touches it again
-            *reinterpret_cast<volatile int*>(&bars->last_arrival) = done;
-          }
-          named_barrier(1, kEpiThreads);
-          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
-          named_barrier(1, kEpiThreads);
-        }
+        // If every other contributor had already published when the check
+        // above ran, this CTA finishes the tile without publishing its own
+        // part (the counter is reset: no other contributor touches it again).
+        // An earlier item of a CTA is almost never the last to arrive.
+        finish = final_item && *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
+        named_barrier(1, kEpiThreads);   // every thread has read the flag
+        if (finish && etid == 0) *counter = 0;
         if (!finish) {
           float4* mine = reinterpret_cast<float4*>(ws_slot(p, cta_of(me), kb0 > 0 ? 0 : 1));
 #pragma unroll 1

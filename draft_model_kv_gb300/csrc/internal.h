@@ -50,6 +50,7 @@ constexpr int kGroupM = 8;     // m-blocks per raster group (L2 reuse of weight 
 constexpr int kTraceWords = 64;      // per CTA: start, end, items, then 6 words per work item
 constexpr int kTraceItems = (kTraceWords - 3) / 6;
 constexpr int kMinUnitsPerCta = 8;   // k-blocks: keeps small problems from over-splitting
+constexpr int kStreamAutoMaxTokens = 64;    // AUTO picks the weight-streaming kernel up to here
 
 size_t tiled_smem_bytes();
 
@@ -87,6 +88,18 @@ cudaError_t launch_tiled(int device, int dtype, int head_dim, bool has_bias, con
 cudaError_t launch_pair(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tmap_x,
                         const CUtensorMap& tmap_w_half, const WriteParams& p, int grid,
                         cudaStream_t stream);
+
+// Weight-streaming kernel for T <= 256 (weights as the MMA's M side).
+// stream_plan: token padding, stage count and TMEM layout for T (false if T is
+// out of range).  launch_stream: grid = CTAs, num_n = weight tiles of 128 rows,
+// num_m = 1; tmap_x box rows = t_pad, tmap_w box 128 rows.
+size_t stream_max_smem_bytes();
+bool stream_plan(int64_t T, int* t_pad, int* stages, uint32_t* stage_b, uint32_t* acc_stride,
+                 uint32_t* tmem_cols);
+cudaError_t launch_stream(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tmap_x,
+                          const CUtensorMap& tmap_w_half, const WriteParams& p, int t_pad, int stages,
+                          uint32_t stage_b, uint32_t acc_stride, uint32_t tmem_cols, int grid,
+                          cudaStream_t stream);
 
 // Number of CTA pairs that can be resident at once on `device` (0 if unknown).
 int pair_workers(int device);

@@ -233,14 +233,20 @@ DSPARK_API int dspark_get_device_status(dspark_bundle_t bundle, void* stream, ui
 /* Reset the device status word to 0 (stream-ordered, asynchronous). */
 DSPARK_API int dspark_clear_device_status(dspark_bundle_t bundle, void* stream);
 
-/* Kernel variant used by later writes with this bundle.  AUTO (the default)
- * and PAIR: 256-token x 256-column tiles computed by two CTAs of a cluster
- * with tcgen05.mma.cta_group::2 (each CTA stages half of the weight tile);
- * SINGLE: 128 x 256 tiles, one CTA each.  Results agree within rounding; the
- * choice only changes speed.  Returns DSPARK_E_INVALID_ARG for other values. */
+/* Kernel variant used by later writes with this bundle.
+ *  PAIR:   256-token x 256-column tiles computed by two CTAs of a cluster with
+ *          tcgen05.mma.cta_group::2 (each CTA stages half of the weight tile).
+ *  SINGLE: 128 x 256 tiles, one CTA each.
+ *  STREAM: for num_tokens <= 256 (and num_kv_heads*head_dim a multiple of 128):
+ *          128 weight rows x all tokens per tile, weights streamed by every SM;
+ *          a write that does not meet those limits returns DSPARK_E_INVALID_ARG.
+ *  AUTO (the default): STREAM when it applies and num_tokens <= 64, else PAIR.
+ * Results agree within rounding; the choice only changes speed.  Returns
+ * DSPARK_E_INVALID_ARG for other values. */
 #define DSPARK_VARIANT_AUTO 0
 #define DSPARK_VARIANT_SINGLE 1
 #define DSPARK_VARIANT_PAIR 2
+#define DSPARK_VARIANT_STREAM 3
 DSPARK_API int dspark_set_kernel_variant(dspark_bundle_t bundle, int32_t variant);
 
 /* Diagnostics: make later writes with this bundle record a per-CTA timeline
