@@ -130,35 +130,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
     tmem_alloc(smem_u32(&bars->tmem_base), cfg.tmem_cols);
     tmem_relinquish();
   }
-  // per-token decisions, shared by every tile of this CTA (all slots are set:
-  // the epilogue reads whole 32-token chunks)
-  for (int t = threadIdx.x; t < kSMaxTokens; t += kSThreads) {
-    int64_t loc = -1, pos = 0;
-    int ok = 0;
-    if (t < p.T) {
-      loc = p.cache_loc[t];
-      ok = loc >= 0;
-      if (ok && p.loc_row_width > 0) {
-        const int64_t b = t / p.loc_row_width;
-        if (t - b * p.loc_row_width >= static_cast<int64_t>(p.commit_lens[b])) ok = 0;
-      }
-      if (ok) {
-        pos = p.positions[t];
-        if (pos < 0 || pos >= p.max_pos) {
-          if (blockIdx.x == 0) flag(p, DSPARK_FLAG_POS_RANGE);
-          ok = 0;
-          pos = 0;
-        } else if (loc >= p.pool_slots) {
-          if (blockIdx.x == 0) flag(p, DSPARK_FLAG_LOC_RANGE);
-          ok = 0;
-          pos = 0;
-        }
-      }
-    }
-    sc->loc[t] = loc;
-    sc->pos[t] = pos;
-    sc->ok[t] = ok;
-  }
   tc_fence_before();
   __syncwarp();
   __syncthreads();
@@ -260,6 +231,33 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Per-token decisions, shared by every tile of this CTA, made while the
+    // producer's first loads are in flight.  Every slot is set: the epilogue
+    // reads whole 32-token chunks.
+    for (int t = threadIdx.x; t < kSMaxTokens; t += kSEpiThreads) {
+      int64_t loc = -1, pos = 0;
+      int ok = 0;
+      if (t < p.T) {
+        // three independent loads, then the decision
+        loc = p.cache_loc[t];
+        pos = p.positions[t];
+        const int64_t w = p.loc_row_width;
+        const int64_t committed = w > 0 ? static_cast<int64_t>(p.commit_lens[t / w]) : 0;
+        ok = loc >= 0 && (w == 0 || t - (t / w) * w < committed);
+        if (ok && (pos < 0 || pos >= p.max_pos)) {
+          if (blockIdx.x == 0) flag(p, DSPARK_FLAG_POS_RANGE);
+          ok = 0;
+        } else if (ok && loc >= p.pool_slots) {
+          if (blockIdx.x == 0) flag(p, DSPARK_FLAG_LOC_RANGE);
+          ok = 0;
+        }
+        if (!ok) pos = 0;
+      }
+      sc->loc[t] = loc;
+      sc->pos[t] = pos;
+      sc->ok[t] = ok;
+    }
+    named_barrier(1, kSEpiThreads);
     constexpr int kHalf = D / 2;
     const int r = threadIdx.x;                 // output feature (TMEM lane) of the tile
     const int d = r % D;                       // element within its head

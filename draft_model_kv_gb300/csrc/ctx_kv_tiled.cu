@@ -295,6 +295,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     regs_increase<kRegsEpilogue>();
     // ------------------------------------------------------------ epilogue
     constexpr int kHalf = D / 2;
+    // cos/sin staging for the last item: measured to pay off for D = 128 only
+    constexpr bool kStageCs = D == 128;
+    constexpr uint32_t kCsBytes = kStageCs ? kTileM * D * 4 : 0;
+    static_assert(kCsBytes <= kRingBytes / 2, "cos/sin staging leaves room for the fixup");
     constexpr int kChunks = kTileN / 32;            // 32-column chunks of a tile
     const int group = warp / 4;                     // warpgroup 0 or 1
     const int quarter = warp % 4;                   // TMEM lanes this warp may read
@@ -380,6 +384,27 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + acc * kAccCols + (static_cast<uint32_t>(quarter * 32) << 16);
 
+      // After the CTA's last MMA the operand ring is idle.  A last item with
+      // 128-wide K heads stages its tokens' cos/sin rows there first (each
+      // group copies half of every row; 16-byte units XOR-swizzled by row so
+      // that the row-per-thread reads below are free of bank conflicts): the
+      // rotation then reads shared memory instead of waiting on L2 per chunk.
+      bool tile_has_k = false;
+      for (int seg = 0; seg < kTileN / D; ++seg) {
+        const int c0 = n_blk * kTileN + seg * D;
+        if (c0 < p.N && c0 % (2 * p.KV) < p.KV) tile_has_k = true;
+      }
+      const bool cs_stage = kStageCs && final_item && tile_has_k;
+      auto stage_cs = [&]() {
+        if (!cs_stage || !write) return;
+        const char* src = reinterpret_cast<const char*>(p.cos_sin + pos * D);
+        const uint32_t dst = smem_u32(smem) + static_cast<uint32_t>(row) * (D * 4);
+        constexpr int kUnits = D / 4;   // 16-byte units per row
+#pragma unroll
+        for (int u = group * (kUnits / 2); u < (group + 1) * (kUnits / 2); ++u)
+          cp_async16(dst + static_cast<uint32_t>((u ^ (row & 7)) * 16), src + u * 16);
+      };
+
       // ---- a tile cut between CTAs: publish this part; the last contributor
       // to arrive adds the other parts into its accumulator and finishes it
       bool finish = true;
@@ -436,6 +461,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           if (finish) tr[3] = global_timer_ns();
         }
         if (finish) {
+          stage_cs();
           // accumulator = sum of all parts in ascending contributor order (this
           // CTA's own part taken from TMEM at its place), so the result does not
           // depend on which contributor arrived last.  Each group sums its half
@@ -447,7 +473,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           // are staged there (each group in its own half) with many asynchronous
           // 16-byte copies in flight; each thread copies, then reads, only its
           // own row.  Otherwise they are read from the workspace directly.
-          constexpr int kHalfRingF4 = kRingBytes / 32;
+          constexpr int kHalfRingF4 = (kRingBytes - kCsBytes) / 32;
           const int per_chunk = n_oth * 8 * rv;           // float4 per column chunk
           const bool staged = final_item && per_chunk <= kHalfRingF4;
           int cpr = kChunks / 2;
@@ -455,8 +481,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             cpr = kHalfRingF4 / per_chunk;                 // >= 1 here
             cpr = cpr > kChunks / 2 ? kChunks / 2 : cpr;
           }
-          const uint32_t ring = smem_u32(smem) + group * kHalfRingF4 * 16;
-          const float4* ring_f4 = reinterpret_cast<const float4*>(smem) + group * kHalfRingF4;
+          const uint32_t ring = smem_u32(smem) + kCsBytes + group * kHalfRingF4 * 16;
+          const float4* ring_f4 = reinterpret_cast<const float4*>(smem + kCsBytes) + group * kHalfRingF4;
 #pragma unroll 1
           for (int ch0 = ch_lo; ch0 < ch_hi; ch0 += cpr) {
             const int nch = (ch_hi - ch0) < cpr ? (ch_hi - ch0) : cpr;
@@ -520,6 +546,11 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         }
       }
 
+      if (!cut) stage_cs();
+      if (cs_stage && finish) {
+        cp_async_wait_all();
+        named_barrier(1, kEpiThreads);   // both halves of every row have landed
+      }
       if (tr != nullptr && finish) tr[4] = global_timer_ns();
       if (finish) {
 #pragma unroll 1
@@ -594,6 +625,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
             const float* w = p.knorm + static_cast<int64_t>(layer) * D;
             const float* cs = p.cos_sin + pos * D;
+            const uint8_t* cs_smem = smem + static_cast<size_t>(row) * (D * 4);
             E* dst = reinterpret_cast<E*>(p.k_pool[layer]) + loc * p.k_stride[layer] + head * D;
             // rotate 16 columns of each half at a time (bounded register use)
 #pragma unroll 1
@@ -614,8 +646,15 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                   const int i = hc * 16 + e4;
                   const float4 w1 = *reinterpret_cast<const float4*>(w + i);
                   const float4 w2 = *reinterpret_cast<const float4*>(w + kHalf + i);
-                  const float4 c4 = *reinterpret_cast<const float4*>(cs + i);
-                  const float4 s4 = *reinterpret_cast<const float4*>(cs + kHalf + i);
+                  float4 c4, s4;
+                  if (cs_stage) {
+                    const int sw = row & 7;
+                    c4 = *reinterpret_cast<const float4*>(cs_smem + ((i / 4) ^ sw) * 16);
+                    s4 = *reinterpret_cast<const float4*>(cs_smem + (((kHalf + i) / 4) ^ sw) * 16);
+                  } else {
+                    c4 = *reinterpret_cast<const float4*>(cs + i);
+                    s4 = *reinterpret_cast<const float4*>(cs + kHalf + i);
+                  }
                   const float wa[4] = {w1.x, w1.y, w1.z, w1.w};
                   const float wb[4] = {w2.x, w2.y, w2.z, w2.w};
                   const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
