@@ -344,6 +344,8 @@ NCU_TRAFFIC = {
     # (workload, tokens) -> per-launch DRAM bytes (read + write) of the fused
     # kernel from one ncu capture of the kernel as it stands (summaries under
     # profiles/); anything without a capture of the current kernel reports null
+    ("decode512", 512): 91.431424e6 + 8.855552e6,
+    ("decode512", 16): 84.098560e6 + 2.786816e6,
 }
 
 
