@@ -354,13 +354,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
                        make_float4(f32(v[4 * j]), f32(v[4 * j + 1]), f32(v[4 * j + 2]), f32(v[4 * j + 3])));
             __syncwarp();
           }
-          __threadfence();
-          named_barrier(1, kSEpiThreads);
+          named_barrier(1, kSEpiThreads);   // every row of the part is written
           if (threadIdx.x == 0) {
-            const int old = atomicAdd(counter, 1);
+            const int old = atom_add_acq_rel_gpu(counter, 1);
             const int last = old == c_last - c_first;
             if (last) *counter = 0;
-            __threadfence();
             *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
           }
           named_barrier(1, kSEpiThreads);

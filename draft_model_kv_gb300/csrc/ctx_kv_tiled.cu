@@ -442,16 +442,14 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             __syncwarp();
           }
           if (tr != nullptr) tr[3] = global_timer_ns();   // dump issued
-          __threadfence();
-          named_barrier(1, kEpiThreads);
-          if (tr != nullptr) tr[4] = global_timer_ns();   // dump visible
+          named_barrier(1, kEpiThreads);                  // every row of the part is written
           if (etid == 0) {
-            const int old = atomicAdd(counter, 1);
+            const int old = atom_add_acq_rel_gpu(counter, 1);
             const int last = old == c_last - c_first;
             if (last) *counter = 0;   // ready for the next launch
-            __threadfence();
             *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
           }
+          if (tr != nullptr) tr[4] = global_timer_ns();   // published
           named_barrier(1, kEpiThreads);
           finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
           named_barrier(1, kEpiThreads);

@@ -366,6 +366,18 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// Arrival on a GPU-scope counter with acquire-release semantics.  Called by
+// one thread after a CTA barrier, the release covers every write that the
+// CTA's threads made before the barrier (release is cumulative), and the
+// acquire makes the parts published by earlier arrivals visible to the CTA
+// after the next barrier.  Much cheaper than a sequentially consistent fence
+// per thread while the memory system is busy streaming operands.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
