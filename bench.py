@@ -50,6 +50,17 @@ def peaks():
                 "source": "fallback"}
 
 
+def written_rows(w):
+    """Tokens whose K and V rows the write stores: loc >= 0 and, in window
+    mode, window column < commit_lens of its row (the roofline's output bytes)."""
+    import numpy as np
+    keep = np.asarray(w.cache_loc) >= 0
+    if w.commit_lens is not None:
+        col = np.arange(w.T) % w.loc_row_width
+        keep &= col < np.repeat(np.asarray(w.commit_lens, dtype=np.int64), w.loc_row_width)
+    return int(keep.sum())
+
+
 def work_per_step(w, written_rows):
     """Algorithmic FLOPs and bytes of one step (DESIGN: roofline accounting)."""
     s = 2
@@ -213,7 +224,6 @@ def run_gpu(args, w):
     import numpy as np
     import torch
     import draft_model_kv_gb300 as dk
-    import oracle
     from draft_model_kv_gb300 import build as _build
     from synthetic.device import stage
 
@@ -227,13 +237,13 @@ def run_gpu(args, w):
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
-    written = oracle.written_tokens(w.cache_loc, w.commit_lens,
-                                    w.loc_row_width if w.commit_lens is not None else None)
+    n_written = written_rows(w)
+    pools = dk.dspark_bind_pools(bundle, st["k_pools"], st["v_pools"])
 
     def step(x=None, pos=None, loc=None, cl=None):
         dk.dspark_write_ctx_kv(bundle, st["ctx_hidden"] if x is None else x,
                                st["positions"] if pos is None else pos, st["cos_sin"],
-                               st["cache_loc"] if loc is None else loc, st["k_pools"], st["v_pools"],
+                               st["cache_loc"] if loc is None else loc, pools,
                                commit_lens=st["commit_lens"] if cl is None else cl,
                                loc_row_width=st["loc_row_width"], stream=stream)
 
@@ -266,29 +276,36 @@ def run_gpu(args, w):
         raise RuntimeError(f"device status flags {flags:#x} during the timed region")
     value, t_max, n_all = aggregate(w.T * args.steps, dev_s)
 
-    # ---- end to end through the public API with pinned host inputs
-    host_x = st["ctx_hidden"].cpu().pin_memory()
-    host_pos = st["positions"].cpu().pin_memory()
-    host_loc = st["cache_loc"].cpu().pin_memory()
-    host_cl = None if st["commit_lens"] is None else st["commit_lens"].cpu().pin_memory()
-    dx = torch.empty_like(st["ctx_hidden"])
-    dpos = torch.empty_like(st["positions"])
-    dloc = torch.empty_like(st["cache_loc"])
-    dcl = None if host_cl is None else torch.empty_like(st["commit_lens"])
-    status_host = ctypes.c_uint32()
-    h2d = host_x.numel() * 2 + host_pos.numel() * 8 + host_loc.numel() * 8 + \
-        (0 if host_cl is None else host_cl.numel() * 4)
+    # ---- end to end through the public API with pinned host inputs: the
+    # step's inputs (hidden, positions, cache_loc, commit_lens) sit in one
+    # pinned host buffer and go to the device in one copy
+    parts = [st["ctx_hidden"], st["positions"], st["cache_loc"]] + \
+        ([] if st["commit_lens"] is None else [st["commit_lens"]])
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=f"cuda:{local}")
+
+    def view(buf, k):
+        t = parts[k]
+        n = t.numel() * t.element_size()
+        return buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+
+    for k, t in enumerate(parts):
+        view(host_buf, k).copy_(t.cpu())
+    dviews = [view(dev_buf, k) for k in range(len(parts))]
+    dx, dpos, dloc = dviews[0], dviews[1], dviews[2]
+    dcl = dviews[3] if len(dviews) > 3 else None
+    h2d = sum(t.numel() * t.element_size() for t in parts)
     e2e_total = 0.0
     e2e_steps = max(1, min(args.steps, 200))
     for i in range(e2e_steps + 3):
         flush.fill_(i & 0xFF)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        dx.copy_(host_x, non_blocking=True)
-        dpos.copy_(host_pos, non_blocking=True)
-        dloc.copy_(host_loc, non_blocking=True)
-        if dcl is not None:
-            dcl.copy_(host_cl, non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         step(dx, dpos, dloc, dcl)
         flags = dk.dspark_get_device_status(bundle, stream)   # d2h of the status word + sync
         t1 = time.perf_counter()
@@ -300,7 +317,7 @@ def run_gpu(args, w):
 
     if rank != 0:
         return None
-    flops, bytes_ = work_per_step(w, len(written))
+    flops, bytes_ = work_per_step(w, n_written)
     pk = peaks()
     mean_ms = statistics.mean(per_step_ms)
     t_tc = flops / (pk["bf16_tflops"] * 1e12)

@@ -21,7 +21,7 @@ __all__ = [
     "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
-    "dspark_set_kernel_variant",
+    "dspark_set_kernel_variant", "dspark_bind_pools", "PoolSet",
     "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
@@ -126,8 +126,43 @@ def _ptr_array(tensors):
     return arr
 
 
+class PoolSet:
+    """Every layer's K and V pool, checked once against a bundle.
+
+    Built by dspark_bind_pools; pass it as `k_pools` (with `v_pools` None) to
+    dspark_write_ctx_kv to skip the per-call checks and pointer marshalling of
+    the pools.  It keeps references to the pool tensors, whose device pointers
+    and row strides it records.
+    """
+    __slots__ = ("k_pools", "v_pools", "k_ptrs", "v_ptrs", "k_strides", "v_strides", "slots",
+                 "dtype_code", "num_layers")
+
+
+def dspark_bind_pools(bundle: Bundle, k_pools, v_pools) -> PoolSet:
+    """Check one [slots, num_kv_heads, head_dim] pool per layer for K and V
+    (head/dim strides (head_dim, 1), one dtype, one slot count) and record
+    their pointers and row strides."""
+    if len(k_pools) != bundle.num_layers or len(v_pools) != bundle.num_layers:
+        raise ValueError("one K and one V pool per layer")
+    slots = k_pools[0].shape[0]
+    for p in list(k_pools) + list(v_pools):
+        if p.dtype != k_pools[0].dtype:
+            raise TypeError("all pools must share one dtype")
+        if (p.dim() != 3 or p.shape[0] != slots or p.shape[1] != bundle.num_kv_heads
+                or p.shape[2] != bundle.head_dim or p.stride(1) != bundle.head_dim or p.stride(2) != 1):
+            raise ValueError("pools must be [slots, num_kv_heads, head_dim] with strides (*, head_dim, 1)")
+    ps = PoolSet()
+    L = bundle.num_layers
+    ps.k_pools, ps.v_pools = tuple(k_pools), tuple(v_pools)
+    ps.k_ptrs, ps.v_ptrs = _ptr_array(k_pools), _ptr_array(v_pools)
+    ps.k_strides = (ctypes.c_int64 * L)(*[p.stride(0) for p in k_pools])
+    ps.v_strides = (ctypes.c_int64 * L)(*[p.stride(0) for p in v_pools])
+    ps.slots, ps.dtype_code, ps.num_layers = slots, _dtype_code(k_pools[0].dtype), L
+    return ps
+
+
 def dspark_write_ctx_kv(bundle: Bundle, ctx_hidden, positions, cos_sin, cache_loc, k_pools,
-                        v_pools, commit_lens=None, loc_row_width: Optional[int] = None,
+                        v_pools=None, commit_lens=None, loc_row_width: Optional[int] = None,
                         stream=None) -> None:
     """Write K (normed, roped) and V of every token into every layer's pool.
 
@@ -135,7 +170,8 @@ def dspark_write_ctx_kv(bundle: Bundle, ctx_hidden, positions, cos_sin, cache_lo
     cache_loc int64 [T]; cos_sin fp32 [max_pos, head_dim]; commit_lens int32
     [bs] with loc_row_width W (bs * W == T) or neither; k_pools / v_pools: one
     [slots, num_kv_heads, head_dim] tensor per layer with head/dim strides
-    (head_dim, 1).  Asynchronous on `stream` (default: torch's current stream).
+    (head_dim, 1), or k_pools a PoolSet from dspark_bind_pools and v_pools
+    None.  Asynchronous on `stream` (default: torch's current stream).
     """
     import torch
     T = ctx_hidden.shape[0]
@@ -147,25 +183,19 @@ def dspark_write_ctx_kv(bundle: Bundle, ctx_hidden, positions, cos_sin, cache_lo
             raise TypeError(f"{name} must be a contiguous {dt} tensor")
     if commit_lens is not None and (commit_lens.dtype != torch.int32 or not commit_lens.is_contiguous()):
         raise TypeError("commit_lens must be a contiguous int32 tensor")
-    if len(k_pools) != bundle.num_layers or len(v_pools) != bundle.num_layers:
-        raise ValueError("one K and one V pool per layer")
-    slots = k_pools[0].shape[0]
-    for p in list(k_pools) + list(v_pools):
-        if p.dtype != k_pools[0].dtype:
-            raise TypeError("all pools must share one dtype")
-        if (p.dim() != 3 or p.shape[0] != slots or p.shape[1] != bundle.num_kv_heads
-                or p.shape[2] != bundle.head_dim or p.stride(1) != bundle.head_dim or p.stride(2) != 1):
-            raise ValueError("pools must be [slots, num_kv_heads, head_dim] with strides (*, head_dim, 1)")
+    if isinstance(k_pools, PoolSet):
+        if v_pools is not None or k_pools.num_layers != bundle.num_layers:
+            raise ValueError("a PoolSet of this bundle's layer count goes alone in k_pools")
+        ps = k_pools
+    else:
+        ps = dspark_bind_pools(bundle, k_pools, v_pools)
     width = 0 if loc_row_width is None else int(loc_row_width)
     nwin = 0 if commit_lens is None else commit_lens.numel()
-    L = bundle.num_layers
-    kstr = (ctypes.c_int64 * L)(*[p.stride(0) for p in k_pools])
-    vstr = (ctypes.c_int64 * L)(*[p.stride(0) for p in v_pools])
     code = load().dspark_write_ctx_kv(
         bundle.handle, ctx_hidden.data_ptr(), T, ctx_hidden.stride(0) if T > 0 else ctx_hidden.shape[1],
         _dtype_code(ctx_hidden.dtype), positions.data_ptr(), cos_sin.data_ptr(), cos_sin.shape[0],
         cache_loc.data_ptr(), None if commit_lens is None else commit_lens.data_ptr(), width, nwin,
-        _ptr_array(k_pools), _ptr_array(v_pools), kstr, vstr, _dtype_code(k_pools[0].dtype), slots,
+        ps.k_ptrs, ps.v_ptrs, ps.k_strides, ps.v_strides, ps.dtype_code, ps.slots,
         _stream_handle(stream))
     _abi.check(code, "dspark_write_ctx_kv")
 

@@ -143,3 +143,23 @@ def test_pack_refusal_needs_no_gpu(lib):
     arr = (_abi.LayerDesc * 2)(desc(), desc(eps=1e-3))
     assert _abi.STATUS[lib.dspark_pack_ctx_kv(arr, 2, 64, None, ctypes.byref(out))] == "E_EPS_MISMATCH"
     assert out.value is None
+
+
+def test_bind_pools_checks_shapes_once():
+    """dspark_bind_pools (host only) refuses pools that do not match the
+    bundle's layers, heads and head_dim, and records pointers and strides."""
+    import types
+    import torch
+    import draft_model_kv_gb300 as dk
+    b = types.SimpleNamespace(handle=None, num_layers=2, num_kv_heads=2, head_dim=64)
+    kp = [torch.zeros(8, 2, 64, dtype=torch.bfloat16) for _ in range(2)]
+    vp = [torch.zeros(8, 2, 64, dtype=torch.bfloat16) for _ in range(2)]
+    ps = dk.dspark_bind_pools(b, kp, vp)
+    assert ps.slots == 8 and ps.num_layers == 2 and list(ps.k_strides) == [128, 128]
+    assert ps.k_ptrs[1] == kp[1].data_ptr()
+    with pytest.raises(ValueError):
+        dk.dspark_bind_pools(b, kp[:1], vp)
+    with pytest.raises(ValueError):
+        dk.dspark_bind_pools(b, kp, [torch.zeros(8, 2, 32, dtype=torch.bfloat16)] * 2)
+    with pytest.raises(TypeError):
+        dk.dspark_bind_pools(b, kp, [torch.zeros(8, 2, 64, dtype=torch.float16)] * 2)

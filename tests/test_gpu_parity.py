@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 import synthetic
-from synthetic.device import sentinel_int16, stage
+from synthetic.device import make_pools, sentinel_int16, stage
 
 pytestmark = pytest.mark.gpu
 
@@ -318,3 +318,25 @@ def test_bundle_info_and_q_rows_never_read():
     slots = torch.from_numpy(w.cache_loc).cuda()
     for p in st["k_pools"] + st["v_pools"]:
         assert torch.isfinite(p[slots].float()).all()
+
+
+def test_bound_pools_write_the_same_bits():
+    """A PoolSet (pools checked and marshalled once) writes exactly what the
+    per-call pool lists write."""
+    import draft_model_kv_gb300 as dk
+    w = workload("decode512", tokens=296)
+    st, b, flags = run_gpu(w)
+    assert flags == 0
+    pools = make_pools(w, "cuda")
+    kp, vp = pools[0::2], pools[1::2]
+    ps = dk.dspark_bind_pools(b, kp, vp)
+    dk.dspark_write_ctx_kv(b, st["ctx_hidden"], st["positions"], st["cos_sin"], st["cache_loc"], ps,
+                           commit_lens=st["commit_lens"], loc_row_width=st["loc_row_width"])
+    torch.cuda.synchronize()
+    assert dk.dspark_get_device_status(b) == 0
+    for got, ref in zip(kp + vp, list(st["k_pools"]) + list(st["v_pools"])):
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    with pytest.raises(ValueError):
+        dk.dspark_write_ctx_kv(b, st["ctx_hidden"], st["positions"], st["cos_sin"], st["cache_loc"], ps,
+                               st["v_pools"], commit_lens=st["commit_lens"],
+                               loc_row_width=st["loc_row_width"])
