@@ -341,6 +341,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
         int32_t* counter = p.counters + c_last;
         // every thread read the early flag before the barrier above
         finish = early;
+        if (final_item && !finish) {
+          // the other parts may have been published while this CTA's MMAs
+          // ran: look again before spending a dump and a fixup read on it
+          if (r == 0) {
+            const int seen = ld_acquire_gpu(counter);
+            *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first;
+          }
+          named_barrier(1, kSEpiThreads);
+          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
+          named_barrier(1, kSEpiThreads);
+        }
         if (finish && r == 0) *counter = 0;   // no other contributor touches it again
         if (!finish) {
           float4* mine = reinterpret_cast<float4*>(ws_slot(p, wid, kb0 > 0 ? 0 : 1));

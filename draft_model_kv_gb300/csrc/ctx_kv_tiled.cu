@@ -423,6 +423,17 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         // An earlier item of a CTA is almost never the last to arrive.
         finish = final_item && *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
         named_barrier(1, kEpiThreads);   // every thread has read the flag
+        if (final_item && !finish) {
+          // the other parts may have been published while this CTA's MMAs
+          // ran: look again before spending a dump and a fixup read on it
+          if (etid == 0) {
+            const int seen = ld_acquire_gpu(counter);
+            *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first;
+          }
+          named_barrier(1, kEpiThreads);
+          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
+          named_barrier(1, kEpiThreads);
+        }
         if (finish && etid == 0) *counter = 0;
         if (!finish) {
           float4* mine = reinterpret_cast<float4*>(ws_slot(p, cta_of(me), kb0 > 0 ? 0 : 1));
