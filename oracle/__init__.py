@@ -12,9 +12,18 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
                          quarter-turn table, hand-worked golden example
   written_tokens         hand-worked window golden example, -1 / commit edge cases
   write_target_hidden_kv composition of the above + bias closed form
+
+and of the in-place QK RMSNorm + table RoPE (``qk_norm_rope.py``, pinned in
+``tests/test_oracle_qknorm_pins.py``):
+  round_to               exhaustive agreement with numpy's float16 conversion
+                         and with bf16 bit truncation plus ties on all patterns
+  table_qk_norm_rope     identity-row closed forms with distinct Q/K weights,
+                         representable identity-row outputs, quarter-turn row,
+                         eps placement, pair norm, exp(i*theta) rotation
 """
 from .ctx_kv import (  # noqa: F401
     LayerDesc, Stacked, WriteArgError, WriteResult, apply_k_norm, apply_k_rope,
     kv_proj_only, layer_descs, per_layer_reference, project_stacked, run_workload,
     stacked_ctx_kv_params, widen, write_target_hidden_kv, written_tokens,
 )
+from .qk_norm_rope import round_to, table_qk_norm_rope  # noqa: F401,E402
