@@ -370,6 +370,124 @@ def ncu_traffic(name, tokens):
     return NCU_TRAFFIC.get((name, tokens))
 
 
+QK_METRIC = "QK-norm+RoPE tokens/s (in place over the Q and K heads of the fused QKV rows)"
+
+
+def run_qk(args):
+    """--op qk_norm_rope: the draft layer's in-place QK RMSNorm + table RoPE
+    (dspark_qk_norm_rope) on the fused QKV rows of the workload's shapes.  A
+    step is one pass over every token's Q and K heads; the L2 is flushed
+    between steps.  HBM roofline: the Q and K heads read and written once,
+    plus a position and a cos/sin row per token."""
+    import numpy as np
+    import torch
+    import synthetic
+    import draft_model_kv_gb300 as dk
+    from draft_model_kv_gb300 import build as _build
+    from synthetic.device import bits_to_tensor
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    _build.build()
+    kw = {} if args.tokens is None else {"tokens": args.tokens}
+    q = synthetic.make_qknorm_workload(args.workload, **kw)
+    dt = torch.bfloat16 if q.dtype == "bf16" else torch.float16
+    dev = f"cuda:{local}"
+    x = bits_to_tensor(q.qkv, dt, dev)
+    pos = torch.from_numpy(q.positions).to(dev)
+    qw, kwt = bits_to_tensor(q.q_weight, dt, dev), bits_to_tensor(q.k_weight, dt, dev)
+    cs = torch.from_numpy(q.cos_sin).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(xx=x, pp=pos):
+        dk.dspark_qk_norm_rope(xx, pp, qw, kwt, cs, q.num_q_heads, q.num_k_heads, q.D, q.eps,
+                               status_flags=status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(SLEEP_CYCLES)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"status flags {int(status.item()):#x}")
+    dev_s = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+    value, t_max, n_all = aggregate(q.T * args.steps, dev_s)
+    nqk = (q.num_q_heads + q.num_k_heads) * q.D
+    bytes_ = q.T * nqk * 2 * 2 + q.T * 8 + q.T * q.D * 4
+    pk = peaks()
+    achieved = bytes_ * args.steps / dev_s / 1e9
+    # end to end: pinned host rows and positions in, the pass, the status word out
+    host_x = x.cpu().pin_memory()
+    host_pos = pos.cpu().pin_memory()
+    e2e_total, e2e_steps = 0.0, max(1, min(args.steps, 100))
+    for i in range(e2e_steps + 3):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        x.copy_(host_x, non_blocking=True)
+        pos.copy_(host_pos, non_blocking=True)
+        step()
+        flag = int(status.item())          # d2h of the status word + sync
+        t1 = time.perf_counter()
+        if i >= 3:
+            e2e_total += t1 - t0
+        if flag:
+            raise RuntimeError(f"status flags {flag:#x} in the e2e loop")
+    e2e_value, _, _ = aggregate(q.T * e2e_steps, e2e_total)
+    if rank != 0:
+        return None
+    out = {
+        "metric": QK_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": q.dtype, "data": "synthetic",
+        "config": {"workload": f"qk_norm_rope/{q.name}", "tokens": q.T, "num_q_heads": q.num_q_heads,
+                   "num_k_heads": q.num_k_heads, "head_dim": q.D, "dtype": q.dtype,
+                   "parallelism": "replicas (one independent pass per GPU, no collective)",
+                   "l2": "flushed between steps (256 MiB write)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": QK_NCU_TRAFFIC.get((q.name, q.T)),
+                     "peak_source": pk["source"]},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": host_x.numel() * 2 + q.T * 8,
+                "d2h_bytes_per_step": 4, "steps": e2e_steps,
+                "timing": "host wall clock per step: h2d rows + positions, the pass, status d2h + sync"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        sample = np.arange(min(q.T, 256))
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds / 2 or reps < 1:
+            oracle.table_qk_norm_rope(q.qkv, q.dtype, q.positions, q.q_weight, q.k_weight, q.cos_sin,
+                                      q.num_q_heads, q.num_k_heads, q.D, q.eps, tokens=sample)
+            reps += 1
+        el = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": len(sample) * reps / el, "unit": UNIT, "cores": host_cores(),
+                               "kind": "oracle", "sample": f"{len(sample)} tokens of {q.name} x {reps} runs, "
+                                                           f"{el:.1f} s, numpy float64"}
+    return out
+
+
+QK_NCU_TRAFFIC = {
+    # (workload, tokens) -> per-launch DRAM bytes of dspark_qk_norm_rope's kernel
+    # from an ncu capture of the kernel as it stands; null without one
+    ("prefill32k", 32768): 341.093888e6 + 274.807552e6,
+}
+
+
 def make(args):
     import synthetic
     kw = {} if args.tokens is None else {"tokens": args.tokens}
@@ -388,6 +506,8 @@ def main(argv=None):
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope"],
+                    help="qk_norm_rope: the draft layers' in-place QK-norm + RoPE instead of the write")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -405,8 +525,10 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-    w = make(args)
-    out = run_gpu(args, w)
+    if args.op == "qk_norm_rope":
+        out = run_qk(args)
+    else:
+        out = run_gpu(args, make(args))
     if out is not None:
         print(json.dumps(out))
     if ws > 1:

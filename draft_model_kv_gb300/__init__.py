@@ -21,7 +21,7 @@ __all__ = [
     "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
-    "dspark_set_kernel_variant", "dspark_bind_pools", "PoolSet",
+    "dspark_set_kernel_variant", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
     "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
@@ -273,6 +273,37 @@ def dspark_write_ctx_kv_noalloc(stacked_weight, k_norm_weight, eps: float, num_l
         _ptr_array(k_pools), _ptr_array(v_pools), kstr, vstr, slots,
         None if status_flags is None else status_flags.data_ptr(), _stream_handle(stream))
     _abi.check(code, "dspark_write_ctx_kv_noalloc")
+
+
+def dspark_qk_norm_rope(qkv, positions, q_weight, k_weight, cos_sin, num_q_heads: int,
+                        num_k_heads: int, head_dim: int, eps: float, status_flags=None,
+                        stream=None) -> None:
+    """In place: RMSNorm (Q or K weight) then table neox RoPE on the first
+    num_q_heads + num_k_heads heads of every row of a fused QKV tensor; the V
+    heads after them are untouched.
+
+    qkv [T, row] bf16 or fp16 (unit column stride, row stride a multiple of 8);
+    positions int64 [T]; q_weight / k_weight [head_dim] in qkv's dtype; cos_sin
+    fp32 [max_pos, head_dim]; status_flags: optional int32 CUDA tensor of one
+    element to which an out-of-table position is reported (that token is left
+    untouched).  Asynchronous on `stream` (default: torch's current stream).
+    """
+    import torch
+    if qkv.dim() != 2 or (qkv.shape[0] > 0 and qkv.stride(1) != 1):
+        raise ValueError("qkv must be [T, row] with unit column stride")
+    if positions.dtype != torch.int64 or not positions.is_contiguous():
+        raise TypeError("positions must be a contiguous int64 tensor")
+    if cos_sin.dtype != torch.float32 or not cos_sin.is_contiguous():
+        raise TypeError("cos_sin must be a contiguous float32 tensor")
+    for name, w in (("q_weight", q_weight), ("k_weight", k_weight)):
+        if w.dtype != qkv.dtype or not w.is_contiguous() or w.numel() != head_dim:
+            raise TypeError(f"{name} must be a contiguous [head_dim] tensor in qkv's dtype")
+    code = load().dspark_qk_norm_rope(
+        qkv.data_ptr(), qkv.shape[0], qkv.stride(0) if qkv.shape[0] > 0 else qkv.shape[1],
+        _dtype_code(qkv.dtype), positions.data_ptr(), q_weight.data_ptr(), k_weight.data_ptr(),
+        cos_sin.data_ptr(), cos_sin.shape[0], num_q_heads, num_k_heads, head_dim, eps,
+        None if status_flags is None else status_flags.data_ptr(), _stream_handle(stream))
+    _abi.check(code, "dspark_qk_norm_rope")
 
 
 def dspark_set_kernel_variant(bundle: Bundle, variant: str) -> None:

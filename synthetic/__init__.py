@@ -245,6 +245,44 @@ def make_workload(name: str, seed: Optional[int] = None, **kw) -> Workload:
 WORKLOADS = ("tiny", "decode512", "prefill32k", "fp16bias", "k3gqa")
 
 
+@dataclasses.dataclass
+class QkWorkload:
+    """Inputs of the in-place QK RMSNorm + table RoPE of one draft layer."""
+    name: str
+    seed: int
+    dtype: str
+    T: int
+    num_q_heads: int
+    num_k_heads: int
+    D: int
+    qkv: np.ndarray          # bits [T, (num_q_heads + 2*num_k_heads) * D]: Q, K, V heads
+    positions: np.ndarray    # int64 [T]
+    cos_sin: np.ndarray      # float32 [max_pos, D]
+    q_weight: np.ndarray     # bits [D]
+    k_weight: np.ndarray     # bits [D]
+    eps: float
+
+    @property
+    def row(self) -> int:
+        return (self.num_q_heads + 2 * self.num_k_heads) * self.D
+
+
+def make_qknorm_workload(name: str, seed: Optional[int] = None, **kw) -> QkWorkload:
+    """The draft layer's fused QKV rows for the shapes of a named context-KV
+    workload: its tokens, positions, cos/sin table, dtype and eps, with
+    q_size / head_dim Q heads and num_kv_heads K and V heads.  QKV values are
+    N(0,1); the Q and K norm weights 1 + 0.1 N(0,1), in the model dtype."""
+    w = make_workload(name, seed, **kw)
+    rng = np.random.default_rng(w.seed + 1000)
+    nq, nk, D = w.q_size // w.D, w.NH, w.D
+    qkv = to_bits(rng.standard_normal((w.T, (nq + 2 * nk) * D), dtype=np.float32), w.dtype)
+    qw = to_bits(1.0 + 0.1 * rng.standard_normal(D, dtype=np.float32), w.dtype)
+    kwt = to_bits(1.0 + 0.1 * rng.standard_normal(D, dtype=np.float32), w.dtype)
+    return QkWorkload(name=name, seed=w.seed, dtype=w.dtype, T=w.T, num_q_heads=nq, num_k_heads=nk, D=D,
+                      qkv=qkv, positions=w.positions, cos_sin=w.cos_sin, q_weight=qw, k_weight=kwt,
+                      eps=w.eps)
+
+
 def describe(w: Workload) -> Dict[str, object]:
     return {"workload": w.name, "tokens": w.T, "hidden": w.H, "layers": w.L,
             "kv_heads": w.NH, "head_dim": w.D, "dtype": w.dtype, "bias": w.has_bias,

@@ -163,3 +163,26 @@ def test_bind_pools_checks_shapes_once():
         dk.dspark_bind_pools(b, kp, [torch.zeros(8, 2, 32, dtype=torch.bfloat16)] * 2)
     with pytest.raises(TypeError):
         dk.dspark_bind_pools(b, kp, [torch.zeros(8, 2, 64, dtype=torch.float16)] * 2)
+
+
+def test_qk_norm_rope_refuses_bad_arguments_before_any_gpu_work(lib):
+    """dspark_qk_norm_rope checks its arguments on the host, before it looks
+    for a device: these refusals need no GPU."""
+    assert "dspark_qk_norm_rope" in declared_symbols()
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    f = lib.dspark_qk_norm_rope
+
+    def call(qkv=base, T=4, stride=1024, dtype=1, pos=base, qw=base, kw=base, cs=base, max_pos=8,
+             nq=4, nk=2, D=128, eps=1e-6):
+        return _abi.STATUS[f(qkv, T, stride, dtype, pos, qw, kw, cs, max_pos, nq, nk, D, eps, None, None)]
+
+    assert call(T=0, qkv=None) == "OK"                       # nothing to do
+    assert call(nq=0, nk=0) == "OK"
+    assert call(D=96) == "E_HEAD_DIM"
+    assert call(dtype=3) == "E_DTYPE_MISMATCH"
+    assert call(T=-1) == "E_INVALID_ARG"
+    assert call(pos=None) == "E_INVALID_ARG"
+    assert call(stride=6 * 128 - 8) == "E_POOL_LAYOUT"       # shorter than the Q and K heads
+    assert call(qkv=base + 2) == "E_ALIGNMENT"
+    assert call(stride=6 * 128 + 4) == "E_ALIGNMENT"
