@@ -20,6 +20,11 @@ and of the in-place QK RMSNorm + table RoPE (``qk_norm_rope.py``, pinned in
   table_qk_norm_rope     identity-row closed forms with distinct Q/K weights,
                          representable identity-row outputs, quarter-turn row,
                          eps placement, pair norm, exp(i*theta) rotation
+
+and of the verify step's accepted-draft count (``verify.py``, pinned in
+``tests/test_oracle_verify_pins.py``):
+  correct_drafts_and_bonus  hand-worked golden cases, suffix independence,
+                            bonus-at-count and all-accepted invariants
 """
 from .ctx_kv import (  # noqa: F401
     LayerDesc, Stacked, WriteArgError, WriteResult, apply_k_norm, apply_k_rope,
@@ -27,3 +32,4 @@ from .ctx_kv import (  # noqa: F401
     stacked_ctx_kv_params, widen, write_target_hidden_kv, written_tokens,
 )
 from .qk_norm_rope import round_to, table_qk_norm_rope  # noqa: F401,E402
+from .verify import correct_drafts_and_bonus  # noqa: F401,E402
