@@ -481,6 +481,95 @@ def run_qk(args):
     return out
 
 
+VERIFY_METRIC = "verify requests/s (accepted-draft count + bonus token per request)"
+
+
+def run_verify(args):
+    """--op verify: dspark_correct_drafts_and_bonus over the workload's
+    requests (batch = tokens / window, block = window; 8 without windows).
+    A step is one launch over the batch; HBM bytes: both int64 token blocks
+    read, the int32 count and int64 bonus written."""
+    import numpy as np
+    import torch
+    import synthetic
+    import draft_model_kv_gb300 as dk
+    from draft_model_kv_gb300 import build as _build
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    _build.build()
+    w = make(args)
+    block = w.loc_row_width or 8
+    batch = max(1, w.T // block)
+    cand, tgt = synthetic.make_verify_workload(batch, block)
+    dev = f"cuda:{local}"
+    dc, dt_ = torch.from_numpy(cand).to(dev), torch.from_numpy(tgt).to(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        dk.dspark_correct_drafts_and_bonus(dc, dt_, stream=stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(SLEEP_CYCLES)
+            starts[i].record(stream)
+            dk.dspark_correct_drafts_and_bonus(dc, dt_, stream=stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    dev_s = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+    value, t_max, _ = aggregate(batch * args.steps, dev_s)
+    bytes_ = batch * block * 8 * 2 + batch * 12
+    pk = peaks()
+    achieved = bytes_ * args.steps / dev_s / 1e9
+    # end to end: pinned host token blocks in, the step, both results out
+    hc, ht = dc.cpu().pin_memory(), dt_.cpu().pin_memory()
+    e2e_total, e2e_steps = 0.0, max(1, min(args.steps, 100))
+    for i in range(e2e_steps + 3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dc.copy_(hc, non_blocking=True)
+        dt_.copy_(ht, non_blocking=True)
+        c, b = dk.dspark_correct_drafts_and_bonus(dc, dt_, stream=stream)
+        c.cpu(), b.cpu()
+        t1 = time.perf_counter()
+        if i >= 3:
+            e2e_total += t1 - t0
+    e2e_value, _, _ = aggregate(batch * e2e_steps, e2e_total)
+    if rank != 0:
+        return None
+    out = {
+        "metric": VERIFY_METRIC, "value": value, "unit": "requests/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+        "config": {"workload": f"verify/{w.name}", "batch": batch, "block": block,
+                   "parallelism": "replicas (one independent step per GPU, no collective)",
+                   "l2": "flushed between steps (256 MiB write)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
+                     "note": "launch-bound: a few KB per launch"},
+        "e2e": {"value": e2e_value, "unit": "requests/s", "h2d_bytes_per_step": batch * block * 16,
+                "d2h_bytes_per_step": batch * 12, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds / 4 or reps < 1:
+            oracle.correct_drafts_and_bonus(cand, tgt)
+            reps += 1
+        el = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": batch * reps / el, "unit": "requests/s", "cores": 1, "kind": "oracle",
+                               "sample": f"{batch} requests x {reps} runs, {el:.1f} s, python loop"}
+    return out
+
+
 QK_NCU_TRAFFIC = {
     # (workload, tokens) -> per-launch DRAM bytes of dspark_qk_norm_rope's kernel
     # from an ncu capture of the kernel as it stands; null without one
@@ -506,8 +595,9 @@ def main(argv=None):
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope"],
-                    help="qk_norm_rope: the draft layers' in-place QK-norm + RoPE instead of the write")
+    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify"],
+                    help="qk_norm_rope: the draft layers' in-place QK-norm + RoPE; verify: the "
+                         "verify step's accepted-draft count and bonus token (instead of the write)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -527,6 +617,8 @@ def main(argv=None):
         dist.init_process_group("nccl")
     if args.op == "qk_norm_rope":
         out = run_qk(args)
+    elif args.op == "verify":
+        out = run_verify(args)
     else:
         out = run_gpu(args, make(args))
     if out is not None:

@@ -22,6 +22,7 @@ __all__ = [
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
     "dspark_set_kernel_variant", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
+    "dspark_correct_drafts_and_bonus",
     "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
@@ -304,6 +305,28 @@ def dspark_qk_norm_rope(qkv, positions, q_weight, k_weight, cos_sin, num_q_heads
         cos_sin.data_ptr(), cos_sin.shape[0], num_q_heads, num_k_heads, head_dim, eps,
         None if status_flags is None else status_flags.data_ptr(), _stream_handle(stream))
     _abi.check(code, "dspark_qk_norm_rope")
+
+
+def dspark_correct_drafts_and_bonus(candidates, target, stream=None):
+    """Per request: how many leading drafts the target accepts, and the
+    target's token after them.  candidates / target: int64 [batch, block] CUDA
+    tensors (unit column stride); candidates[:, 0] is the last verified token.
+    Returns (correct int32 [batch], bonus int64 [batch]) on the same device."""
+    import torch
+    for name, t in (("candidates", candidates), ("target", target)):
+        if t.dtype != torch.int64 or t.dim() != 2 or (t.numel() and t.stride(1) != 1):
+            raise TypeError(f"{name} must be an int64 [batch, block] tensor with unit column stride")
+    if candidates.shape != target.shape:
+        raise ValueError("candidates and target must have the same shape")
+    batch, block = candidates.shape
+    correct = torch.empty(batch, dtype=torch.int32, device=candidates.device)
+    bonus = torch.empty(batch, dtype=torch.int64, device=candidates.device)
+    code = load().dspark_correct_drafts_and_bonus(
+        candidates.data_ptr(), candidates.stride(0) if batch else block, target.data_ptr(),
+        target.stride(0) if batch else block, batch, block, correct.data_ptr(), bonus.data_ptr(),
+        _stream_handle(stream))
+    _abi.check(code, "dspark_correct_drafts_and_bonus")
+    return correct, bonus
 
 
 def dspark_set_kernel_variant(bundle: Bundle, variant: str) -> None:

@@ -288,3 +288,20 @@ def describe(w: Workload) -> Dict[str, object]:
             "kv_heads": w.NH, "head_dim": w.D, "dtype": w.dtype, "bias": w.has_bias,
             "window": w.loc_row_width, "pool_slots": w.pool_slots, "max_pos": w.max_pos,
             "seed": w.seed}
+
+
+def make_verify_workload(batch: int, block: int, seed: int = 5, vocab: int = 151936):
+    """Verify-step inputs: int64 target [batch, block] uniform over the vocab;
+    candidates [batch, block] whose column 0 is random and whose drafts copy
+    the target's previous-position token up to a first disagreement at a
+    uniform position in [0, block-1] (block-1: every draft agrees); the
+    tokens after it are random."""
+    rng = np.random.default_rng(seed)
+    target = rng.integers(0, vocab, size=(batch, block), dtype=np.int64)
+    cand = rng.integers(0, vocab, size=(batch, block), dtype=np.int64)
+    k = rng.integers(0, block, size=batch)
+    for b in range(batch):
+        cand[b, 1:k[b] + 1] = target[b, :k[b]]
+        if k[b] < block - 1:
+            cand[b, k[b] + 1] = (target[b, k[b]] + 1 + rng.integers(0, vocab - 1)) % vocab
+    return cand, target

@@ -186,3 +186,19 @@ def test_qk_norm_rope_refuses_bad_arguments_before_any_gpu_work(lib):
     assert call(stride=6 * 128 - 8) == "E_POOL_LAYOUT"       # shorter than the Q and K heads
     assert call(qkv=base + 2) == "E_ALIGNMENT"
     assert call(stride=6 * 128 + 4) == "E_ALIGNMENT"
+
+
+def test_correct_drafts_refuses_bad_arguments_before_any_gpu_work(lib):
+    buf = ctypes.create_string_buffer(1024)
+    p = ctypes.addressof(buf)
+    f = lib.dspark_correct_drafts_and_bonus
+
+    def call(c=p, cs=8, t=p, ts=8, batch=4, block=8, out_c=p, out_b=p):
+        return _abi.STATUS[f(c, cs, t, ts, batch, block, out_c, out_b, None)]
+
+    assert call(batch=0, c=None) == "OK"
+    assert call(block=0) == "E_INVALID_ARG"
+    assert call(batch=-1) == "E_INVALID_ARG"
+    assert call(cs=7) == "E_INVALID_ARG"
+    assert call(t=None) == "E_INVALID_ARG"
+    assert call(out_b=None) == "E_INVALID_ARG"
