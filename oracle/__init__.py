@@ -25,6 +25,13 @@ and of the verify step's accepted-draft count (``verify.py``, pinned in
 ``tests/test_oracle_verify_pins.py``):
   correct_drafts_and_bonus  hand-worked golden cases, suffix independence,
                             bonus-at-count and all-accepted invariants
+
+and of the draft attention over the pool (``draft_attention.py``, pinned in
+``tests/test_oracle_attention_pins.py``):
+  draft_attention        single key, equal keys (mean of values), per-KV-head
+                         constant values (GQA head mapping), two-key weight
+                         ratio exp(sm_scale * diff), non-causal extend keys,
+                         key permutation invariance, dominant key
 """
 from .ctx_kv import (  # noqa: F401
     LayerDesc, Stacked, WriteArgError, WriteResult, apply_k_norm, apply_k_rope,
@@ -33,3 +40,4 @@ from .ctx_kv import (  # noqa: F401
 )
 from .qk_norm_rope import round_to, table_qk_norm_rope  # noqa: F401,E402
 from .verify import correct_drafts_and_bonus  # noqa: F401,E402
+from .draft_attention import draft_attention  # noqa: F401,E402
