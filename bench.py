@@ -570,6 +570,138 @@ def run_verify(args):
     return out
 
 
+ATTN_METRIC = "draft attention query tokens/s (GQA over the pool, non-causal block, split-KV)"
+
+
+def run_attention(args):
+    """--op attention: dspark_draft_attention for the decode512 request mix:
+    64 requests x 8-token blocks, context U[1024, 32768] per request from a
+    pool of the total context (random slot order), 32 query / 8 KV heads of
+    128, bf16.  Pools, queries and block keys are drawn on the device from a
+    seeded generator.  HBM roofline: every context K and V row once, its slot
+    index, the block's q / k / v and the output."""
+    import numpy as np
+    import torch
+    import draft_model_kv_gb300 as dk
+    from draft_model_kv_gb300 import build as _build
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = f"cuda:{local}"
+    batch, block, nq, nkv, D = 64, 8, 32, 8, 128
+    rng = np.random.default_rng(9)
+    ctx = rng.integers(1024, 32768 + 1, size=batch)
+    if args.tokens is not None:                    # supplementary: a fixed context length
+        ctx = np.full(batch, args.tokens)
+    slots = int(ctx.sum()) + 64
+    gen = torch.Generator(device=dev).manual_seed(9)
+    rows = batch * block
+    q = torch.randn((rows, nq, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    ke = torch.randn((rows, nkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    ve = torch.randn((rows, nkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    kp = torch.randn((slots, nkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    vp = torch.randn((slots, nkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    idx = torch.randperm(slots, generator=gen, device=dev)[:int(ctx.sum())].contiguous()
+    start = torch.from_numpy(np.concatenate([[0], np.cumsum(ctx)]).astype(np.int64)).to(dev)
+    max_ctx = int(ctx.max())
+    out = torch.empty_like(q)
+    wsb = dk.dspark_draft_attention_workspace_bytes(batch, block, nq, nkv, D, max_ctx)
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = D ** -0.5
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        dk.dspark_draft_attention(q, ke, ve, kp, vp, idx, start, scale, max_ctx, out=out, workspace=work,
+                                  status_flags=status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(SLEEP_CYCLES)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"status flags {int(status.item()):#x}")
+    dev_s = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3
+    value, t_max, _ = aggregate(rows * args.steps, dev_s)
+    ctx_total = int(ctx.sum())
+    bytes_ = ctx_total * (nkv * D * 2 * 2 + 8) + rows * (nq + 2 * nkv) * D * 2 + rows * nq * D * 2
+    pk = peaks()
+    achieved = bytes_ * args.steps / dev_s / 1e9
+    # end to end: the block's q / k / v from pinned host memory, the attention, the output back
+    hq, hk, hv = q.cpu().pin_memory(), ke.cpu().pin_memory(), ve.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_total, e2e_steps = 0.0, max(1, min(args.steps, 50))
+    for i in range(e2e_steps + 3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        q.copy_(hq, non_blocking=True)
+        ke.copy_(hk, non_blocking=True)
+        ve.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        if i >= 3:
+            e2e_total += t1 - t0
+    e2e_value, _, _ = aggregate(rows * e2e_steps, e2e_total)
+    if rank != 0:
+        return None
+    res = {
+        "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "draft_attention/decode512", "requests": batch, "block": block,
+                   "num_q_heads": nq, "num_kv_heads": nkv, "head_dim": D, "context_tokens": ctx_total,
+                   "max_context": max_ctx, "parallelism": "replicas (one independent pass per GPU, no collective)",
+                   "l2": "flushed between steps (256 MiB write); inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": ATTN_NCU_TRAFFIC.get((batch, ctx_total)),
+                     "peak_source": pk["source"]},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": rows * (nq + 2 * nkv) * D * 2,
+                "d2h_bytes_per_step": rows * nq * D * 2, "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        b = int(np.argmin(ctx))                      # one request, its rows copied back
+        sl = idx[int(start[b]):int(start[b + 1])]
+        lo_bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+        sub_k, sub_v = lo_bits(kp[sl]), lo_bits(vp[sl])
+        qb, keb, veb = (lo_bits(t[b * block:(b + 1) * block]) for t in (q, ke, ve))
+        local_idx = np.arange(ctx[b], dtype=np.int64)
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds / 2 or reps < 1:
+            oracle.draft_attention(qb, keb, veb, sub_k, sub_v, local_idx, np.array([0, ctx[b]]), "bf16", nq,
+                                   nkv, D, scale)
+            reps += 1
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": block * reps / el, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                               "sample": f"one request ({ctx[b]} context tokens) x {reps} runs, {el:.1f} s, "
+                                         f"numpy float64"}
+    return res
+
+
+ATTN_NCU_TRAFFIC = {
+    # (requests, total context tokens) -> per-launch DRAM bytes of the split
+    # kernel from an ncu capture of the kernel as it stands; null without one
+}
+
+
 QK_NCU_TRAFFIC = {
     # (workload, tokens) -> per-launch DRAM bytes of dspark_qk_norm_rope's kernel
     # from an ncu capture of the kernel as it stands; null without one
@@ -595,7 +727,7 @@ def main(argv=None):
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify"],
+    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify", "attention"],
                     help="qk_norm_rope: the draft layers' in-place QK-norm + RoPE; verify: the "
                          "verify step's accepted-draft count and bonus token (instead of the write)")
     args = ap.parse_args(argv)
@@ -619,6 +751,8 @@ def main(argv=None):
         out = run_qk(args)
     elif args.op == "verify":
         out = run_verify(args)
+    elif args.op == "attention":
+        out = run_attention(args)
     else:
         out = run_gpu(args, make(args))
     if out is not None:

@@ -22,7 +22,7 @@ __all__ = [
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
     "dspark_set_kernel_variant", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
-    "dspark_correct_drafts_and_bonus",
+    "dspark_correct_drafts_and_bonus", "dspark_draft_attention", "dspark_draft_attention_workspace_bytes",
     "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
@@ -327,6 +327,53 @@ def dspark_correct_drafts_and_bonus(candidates, target, stream=None):
         _stream_handle(stream))
     _abi.check(code, "dspark_correct_drafts_and_bonus")
     return correct, bonus
+
+
+def dspark_draft_attention_workspace_bytes(batch: int, block: int, num_q_heads: int, num_kv_heads: int,
+                                           head_dim: int, max_context: int) -> int:
+    """Workspace bytes dspark_draft_attention needs (0: unsupported sizes)."""
+    return int(load().dspark_draft_attention_workspace_bytes(batch, block, num_q_heads, num_kv_heads, head_dim,
+                                                             max_context))
+
+
+def dspark_draft_attention(q, k_ext, v_ext, k_pool, v_pool, kv_indices, kv_start, sm_scale: float,
+                           max_context: int, out=None, workspace=None, status_flags=None, stream=None):
+    """Non-causal GQA attention of each request's draft block over its
+    context in the pool (kv_indices[kv_start[b]:kv_start[b+1]]) and the block's
+    own keys.  q [batch*block, Hq, D]; k_ext / v_ext [batch*block, Hkv, D];
+    k_pool / v_pool [slots, Hkv, D] (row stride a multiple of 8); kv_indices /
+    kv_start int64 CUDA tensors; max_context bounds every context length.
+    Returns out [batch*block, Hq, D] (allocated when not given); the workspace
+    is allocated when not given (dspark_draft_attention_workspace_bytes)."""
+    import torch
+    nq, D = q.shape[1], q.shape[2]
+    nkv = k_ext.shape[1]
+    batch = kv_start.numel() - 1
+    block = q.shape[0] // batch if batch > 0 else 1
+    for name, t in (("q", q), ("k_ext", k_ext), ("v_ext", v_ext), ("out", out)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool)):
+        if t.dim() != 3 or t.shape[1] != nkv or t.shape[2] != D or t.stride(1) != D or t.stride(2) != 1:
+            raise ValueError(f"{name} must be [slots, num_kv_heads, head_dim] with strides (*, head_dim, 1)")
+    if k_pool.stride(0) != v_pool.stride(0) or k_pool.shape[0] != v_pool.shape[0]:
+        raise ValueError("k_pool and v_pool must share slots and row stride")
+    for name, t in (("kv_indices", kv_indices), ("kv_start", kv_start)):
+        if t.dtype != torch.int64 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int64 tensor")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = dspark_draft_attention_workspace_bytes(max(batch, 1), block, nq, nkv, D, max_context)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    code = load().dspark_draft_attention(
+        q.data_ptr(), k_ext.data_ptr(), v_ext.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), k_pool.stride(0),
+        k_pool.shape[0], kv_indices.data_ptr(), kv_start.data_ptr(), batch, block, nq, nkv, D,
+        _dtype_code(q.dtype), sm_scale, max_context, out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), None if status_flags is None else status_flags.data_ptr(),
+        _stream_handle(stream))
+    _abi.check(code, "dspark_draft_attention")
+    return out
 
 
 def dspark_set_kernel_variant(bundle: Bundle, variant: str) -> None:

@@ -110,6 +110,11 @@ def load() -> ctypes.CDLL:
     lib.dspark_qk_norm_rope.restype = ctypes.c_int
     lib.dspark_correct_drafts_and_bonus.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp, vp]
     lib.dspark_correct_drafts_and_bonus.restype = ctypes.c_int
+    lib.dspark_draft_attention_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i64]
+    lib.dspark_draft_attention_workspace_bytes.restype = i64
+    lib.dspark_draft_attention.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp, vp, i64, i32, i32, i32, i32, i32,
+                                           ctypes.c_float, i64, vp, vp, i64, vp, vp]
+    lib.dspark_draft_attention.restype = ctypes.c_int
     lib.dspark_status_string.argtypes = [ctypes.c_int]
     lib.dspark_status_string.restype = ctypes.c_char_p
     _lib = lib

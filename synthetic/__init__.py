@@ -305,3 +305,49 @@ def make_verify_workload(batch: int, block: int, seed: int = 5, vocab: int = 151
         if k[b] < block - 1:
             cand[b, k[b] + 1] = (target[b, k[b]] + 1 + rng.integers(0, vocab - 1)) % vocab
     return cand, target
+
+
+@dataclasses.dataclass
+class AttnWorkload:
+    """Inputs of the draft attention over a pool (bit patterns in ``dtype``)."""
+    dtype: str
+    batch: int
+    block: int
+    num_q_heads: int
+    num_kv_heads: int
+    D: int
+    q: np.ndarray            # [batch*block, Hq, D]
+    k_ext: np.ndarray        # [batch*block, Hkv, D]
+    v_ext: np.ndarray
+    k_pool: np.ndarray       # [slots, Hkv, D]
+    v_pool: np.ndarray
+    kv_indices: np.ndarray   # int64 [sum of context lengths]
+    kv_start: np.ndarray     # int64 [batch + 1]
+    sm_scale: float
+
+    @property
+    def max_context(self) -> int:
+        return int(np.diff(self.kv_start).max()) if self.batch else 0
+
+
+def make_attention_workload(batch: int, block: int, num_q_heads: int, num_kv_heads: int, D: int,
+                            ctx_lo: int, ctx_hi: int, slack: int = 64, dtype: str = BF16,
+                            seed: int = 6) -> AttnWorkload:
+    """Per request a context length U[ctx_lo, ctx_hi] of distinct random pool
+    slots (pool = total context + slack slots); q, keys and values N(0,1) in
+    the model dtype; sm_scale = D**-0.5."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(ctx_lo, ctx_hi + 1, size=batch)
+    slots = int(ctx.sum()) + slack
+    idx = rng.permutation(slots)[:int(ctx.sum())].astype(np.int64)
+    start = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int64)
+    rows = batch * block
+
+    def draw(*shape):
+        return to_bits(rng.standard_normal(shape, dtype=np.float32), dtype)
+
+    return AttnWorkload(dtype=dtype, batch=batch, block=block, num_q_heads=num_q_heads,
+                        num_kv_heads=num_kv_heads, D=D, q=draw(rows, num_q_heads, D),
+                        k_ext=draw(rows, num_kv_heads, D), v_ext=draw(rows, num_kv_heads, D),
+                        k_pool=draw(slots, num_kv_heads, D), v_pool=draw(slots, num_kv_heads, D),
+                        kv_indices=idx, kv_start=start, sm_scale=float(D) ** -0.5)

@@ -202,3 +202,28 @@ def test_correct_drafts_refuses_bad_arguments_before_any_gpu_work(lib):
     assert call(cs=7) == "E_INVALID_ARG"
     assert call(t=None) == "E_INVALID_ARG"
     assert call(out_b=None) == "E_INVALID_ARG"
+
+
+def test_draft_attention_sizes_and_refusals_need_no_gpu(lib):
+    """The workspace size query and the shape refusals run on the host."""
+    ws = lib.dspark_draft_attention_workspace_bytes
+    assert ws(64, 8, 32, 8, 128, 32768) > 0
+    assert ws(64, 8, 32, 8, 96, 1000) == 0          # head_dim
+    assert ws(64, 8, 30, 8, 128, 1000) == 0         # heads not grouped
+    assert ws(64, 3, 32, 8, 128, 1000) == 0         # 12 rows per KV head
+    assert ws(64, 16, 32, 8, 128, 1000) == 0        # 64 rows per KV head x 8 heads: 32 warps
+    f = lib.dspark_draft_attention
+    buf = ctypes.create_string_buffer(64)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16
+
+    def call(D=128, dtype=1, block=8, nq=32, nkv=8, stride=1024, wsb=1 << 30, q=p):
+        return _abi.STATUS[f(q, p, p, p, p, stride, 100, p, p, 4, block, nq, nkv, D, dtype, 0.1, 64, p, p, wsb,
+                             None, None)]
+
+    assert call(D=96) == "E_HEAD_DIM"
+    assert call(dtype=3) == "E_DTYPE_MISMATCH"
+    assert call(block=3) == "E_SHAPE_MISMATCH"
+    assert call(stride=1000) == "E_POOL_LAYOUT"
+    assert call(stride=1028) == "E_ALIGNMENT"
+    assert call(q=p + 4) == "E_ALIGNMENT"
+    assert call(wsb=16) == "E_SCRATCH_LIMIT"
