@@ -236,13 +236,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) attn_split_kernel(const Att
     }
   }
 
+  const bool units_fixed = nthreads % units_row == 0;
+  const int my_u = tid % units_row, my_j0 = tid / units_row, j_step = nthreads / units_row;
   auto issue = [&](int ci, int stage) {
     uint8_t* ks = kv_s + stage * L.stage_bytes;
     uint8_t* vs = ks + kChunk * L.row_bytes;
     const E* kbase;
     const E* vbase;
-    for (int x = tid; x < kChunk * units_row; x += nthreads) {
-      const int j = x / units_row, u = x % units_row;
+    auto copy_unit = [&](int j, int u) {
       bool ok;
       int64_t row_off;
       if (ci < ext_chunks) {
@@ -272,6 +273,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) attn_split_kernel(const Att
         *reinterpret_cast<uint4*>(vs + off) = make_uint4(0u, 0u, 0u, 0u);
       }
       if (u == 0) valid_s[stage * kChunk + j] = ok ? 1 : 0;
+    };
+    if (units_fixed) {
+      // the usual case: each thread copies one fixed 16-byte unit of every
+      // j_step-th token row (no integer division per unit)
+      for (int j = my_j0; j < kChunk; j += j_step) copy_unit(j, my_u);
+    } else {
+      for (int x = tid; x < kChunk * units_row; x += nthreads) copy_unit(x / units_row, x % units_row);
     }
     cp_async_commit();
   };
@@ -319,10 +327,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) attn_split_kernel(const Att
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
+        const int2 vk = *reinterpret_cast<const int2*>(valid_s + stage * kChunk + nt * 8 + 2 * tig);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int key = nt * 8 + 2 * tig + e;
-          const bool ok = valid_s[stage * kChunk + key] != 0;
+          const bool ok = (e == 0 ? vk.x : vk.y) != 0;
           sc[nt][e] = ok ? sc[nt][e] * p.scale_log2 : -INFINITY;
           sc[nt][2 + e] = ok ? sc[nt][2 + e] * p.scale_log2 : -INFINITY;
           mx0 = fmaxf(mx0, sc[nt][e]);
