@@ -42,17 +42,18 @@ struct AttnPlan {
   int split_tokens;
 };
 
-// Context split: about kSplitGoal tokens per split, at least four waves of
-// CTAs, and among up to twice that many splits the count whose CTAs fill the
-// last wave best (a request's unused splits end at once, so this matters for
+// Context split: about kSplitGoal tokens per split, at least two waves of
+// CTAs (more splits cost workspace traffic and merge work: measured slower),
+// and among up to twice that many splits the count whose CTAs fill the last
+// wave best (a request's unused splits end at once, so this matters for
 // equal context lengths).  Depends on the sizes only, so the workspace size
 // query and the launch agree.
 AttnPlan make_plan(int64_t batch, int64_t max_context) {
   AttnPlan pl;
   if (batch < 1) batch = 1;
   int64_t base = (max_context + kSplitGoal - 1) / kSplitGoal;
-  const int64_t waves4 = (4 * kWaveCtas + batch - 1) / batch;
-  if (base < waves4) base = waves4;
+  const int64_t waves2 = (2 * kWaveCtas + batch - 1) / batch;
+  if (base < waves2) base = waves2;
   if (base < 1) base = 1;
   int64_t best = base;
   double best_eff = 0.0;
