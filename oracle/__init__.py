@@ -32,6 +32,12 @@ and of the draft attention over the pool (``draft_attention.py``, pinned in
                          constant values (GQA head mapping), two-key weight
                          ratio exp(sm_scale * diff), non-causal extend keys,
                          key permutation invariance, dominant key
+
+and of the draft model's combine_hidden_states (``combine.py``, pinned in
+``tests/test_oracle_combine_pins.py``):
+  combine_hidden_states  identity-block weight closed form (sign(c) * w on
+                         constant rows), one-hot columns, scale invariance,
+                         mean-square invariant, representable rounding of y
 """
 from .ctx_kv import (  # noqa: F401
     LayerDesc, Stacked, WriteArgError, WriteResult, apply_k_norm, apply_k_rope,
@@ -41,3 +47,4 @@ from .ctx_kv import (  # noqa: F401
 from .qk_norm_rope import round_to, table_qk_norm_rope  # noqa: F401,E402
 from .verify import correct_drafts_and_bonus  # noqa: F401,E402
 from .draft_attention import draft_attention  # noqa: F401,E402
+from .combine import combine_hidden_states  # noqa: F401,E402
