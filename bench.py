@@ -696,6 +696,113 @@ def run_attention(args):
     return res
 
 
+COMBINE_METRIC = "combine_hidden_states tokens/s (main_proj GEMM + main_norm)"
+
+
+def run_combine(args):
+    """--op combine: dspark_combine_hidden_states on the workload's shapes
+    (3 auxiliary hidden states of the target: aux_dim = 3 x hidden).  Tensor
+    roofline: 2 x T x hidden x aux_dim FLOP; HBM: main_proj weight, aux,
+    and ctx_hidden written, read and rewritten by the norm pass."""
+    import numpy as np
+    import torch
+    import synthetic
+    import draft_model_kv_gb300 as dk
+    from draft_model_kv_gb300 import build as _build
+    from synthetic.device import bits_to_tensor
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = f"cuda:{local}"
+    cw = synthetic.make_combine_workload(args.workload, tokens=args.tokens)
+    dt = torch.bfloat16 if cw.dtype == "bf16" else torch.float16
+    W = bits_to_tensor(cw.weight, dt, dev)
+    c = dk.dspark_pack_combine(W, bits_to_tensor(cw.norm_weight, dt, dev), cw.eps)
+    aux = bits_to_tensor(cw.aux, dt, dev)
+    out = torch.empty((cw.T, cw.hidden), dtype=dt, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        dk.dspark_combine_hidden_states(c, aux, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(SLEEP_CYCLES)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    if dk.dspark_combine_get_status(c):
+        raise RuntimeError("combine status flags set")
+    dev_s = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3
+    value, t_max, _ = aggregate(cw.T * args.steps, dev_s)
+    K = cw.n_aux * cw.hidden
+    flops = 2.0 * cw.T * cw.hidden * K
+    bytes_ = cw.hidden * K * 2 + cw.T * K * 2 + 3 * cw.T * cw.hidden * 2
+    pk = peaks()
+    t_step = dev_s / args.steps
+    hx = aux.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=dt).pin_memory()
+    e2e_total, e2e_steps = 0.0, max(1, min(args.steps, 100))
+    for i in range(e2e_steps + 3):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        aux.copy_(hx, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        if i >= 3:
+            e2e_total += t1 - t0
+    e2e_value, _, _ = aggregate(cw.T * e2e_steps, e2e_total)
+    if rank != 0:
+        return None
+    tensor = {"bound": "tensor", "achieved": flops / t_step / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+              "frac": flops / t_step / 1e12 / pk["bf16_tflops"], "traffic": None,
+              "peak_source": pk["source"] + " (burst: the kernel is timed alone)"}
+    hbm = {"bound": "hbm", "achieved": bytes_ / t_step / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+           "frac": bytes_ / t_step / 1e9 / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"]}
+    t_tc, t_hbm = flops / (pk["bf16_tflops"] * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9)
+    primary, other = (tensor, hbm) if t_tc >= t_hbm else (hbm, tensor)
+    res = {
+        "metric": COMBINE_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cw.dtype, "data": "synthetic",
+        "config": {"workload": f"combine/{args.workload}", "tokens": cw.T, "hidden": cw.hidden, "aux_dim": K,
+                   "parallelism": "replicas (one independent pass per GPU, no collective)",
+                   "l2": "flushed between steps (256 MiB write)"},
+        "roofline": primary, "roofline_other": other, "roofline_time_frac": max(t_tc, t_hbm) / t_step,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cw.T * K * 2,
+                "d2h_bytes_per_step": cw.T * cw.hidden * 2, "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        rows = min(cw.T, 64)
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds / 2 or reps < 1:
+            oracle.combine_hidden_states(cw.aux[:rows], cw.weight, cw.norm_weight, cw.eps, cw.dtype)
+            reps += 1
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": rows * reps / el, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                               "sample": f"{rows} tokens x {reps} runs, {el:.1f} s, numpy float64"}
+    c.free()
+    return res
+
+
 ATTN_NCU_TRAFFIC = {
     # (requests, total context tokens) -> per-launch DRAM bytes of the split
     # kernel from an ncu capture of the kernel as it stands; null without one
@@ -727,7 +834,7 @@ def main(argv=None):
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify", "attention"],
+    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify", "attention", "combine"],
                     help="qk_norm_rope: the draft layers' in-place QK-norm + RoPE; verify: the "
                          "verify step's accepted-draft count and bonus token (instead of the write)")
     args = ap.parse_args(argv)
@@ -753,6 +860,8 @@ def main(argv=None):
         out = run_verify(args)
     elif args.op == "attention":
         out = run_attention(args)
+    elif args.op == "combine":
+        out = run_combine(args)
     else:
         out = run_gpu(args, make(args))
     if out is not None:

@@ -23,6 +23,7 @@ __all__ = [
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
     "dspark_set_kernel_variant", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
     "dspark_correct_drafts_and_bonus", "dspark_draft_attention", "dspark_draft_attention_workspace_bytes",
+    "Combine", "dspark_pack_combine", "dspark_combine_hidden_states", "dspark_combine_get_status",
     "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
@@ -374,6 +375,71 @@ def dspark_draft_attention(q, k_ext, v_ext, k_pool, v_pool, kv_indices, kv_start
         _stream_handle(stream))
     _abi.check(code, "dspark_draft_attention")
     return out
+
+
+class Combine:
+    """Handle of dspark_pack_combine (main_proj / main_norm of the draft
+    model); keeps the main_proj weight tensor alive, as the library does not
+    copy it."""
+
+    def __init__(self, handle, weight, hidden: int, aux_dim: int, dtype):
+        self.handle = handle
+        self.weight = weight
+        self.hidden = hidden
+        self.aux_dim = aux_dim
+        self.dtype = dtype
+
+    def free(self) -> None:
+        if self.handle:
+            load().dspark_free_combine(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def dspark_pack_combine(main_proj_weight, main_norm_weight, eps: float, stream=None) -> Combine:
+    """main_proj_weight [hidden, aux_dim] (bf16 / fp16, unit column stride),
+    main_norm_weight [hidden] (bf16 / fp16 / fp32)."""
+    w = main_proj_weight
+    if w.dim() != 2 or w.stride(1) != 1:
+        raise ValueError("main_proj_weight must be [hidden, aux_dim] with unit column stride")
+    if main_norm_weight.numel() != w.shape[0] or not main_norm_weight.is_contiguous():
+        raise ValueError("main_norm_weight must be a contiguous [hidden] tensor")
+    out = ctypes.c_void_p()
+    code = load().dspark_pack_combine(w.data_ptr(), w.shape[0], w.shape[1], w.stride(0), _dtype_code(w.dtype),
+                                      main_norm_weight.data_ptr(), _dtype_code(main_norm_weight.dtype), eps,
+                                      _stream_handle(stream), ctypes.byref(out))
+    _abi.check(code, "dspark_pack_combine")
+    return Combine(out.value, w, w.shape[0], w.shape[1], w.dtype)
+
+
+def dspark_combine_hidden_states(c: Combine, aux, out=None, stream=None):
+    """ctx_hidden = main_norm(main_proj(aux)); aux [T, aux_dim] in the handle's
+    dtype.  Returns out [T, hidden] (allocated when not given)."""
+    import torch
+    if aux.dim() != 2 or aux.shape[1] != c.aux_dim or (aux.shape[0] and aux.stride(1) != 1):
+        raise ValueError("aux must be [T, aux_dim] with unit column stride")
+    if aux.dtype != c.dtype:
+        raise TypeError("aux must be in the handle's dtype")
+    if out is None:
+        out = torch.empty((aux.shape[0], c.hidden), dtype=aux.dtype, device=aux.device)
+    code = load().dspark_combine_hidden_states(c.handle, aux.data_ptr(), aux.shape[0],
+                                               aux.stride(0) if aux.shape[0] else c.aux_dim, out.data_ptr(),
+                                               out.stride(0) if out.shape[0] else c.hidden,
+                                               _stream_handle(stream))
+    _abi.check(code, "dspark_combine_hidden_states")
+    return out
+
+
+def dspark_combine_get_status(c: Combine, stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    _abi.check(load().dspark_combine_get_status(c.handle, _stream_handle(stream), ctypes.byref(flags)),
+               "dspark_combine_get_status")
+    return flags.value
 
 
 def dspark_set_kernel_variant(bundle: Bundle, variant: str) -> None:

@@ -115,6 +115,14 @@ def load() -> ctypes.CDLL:
     lib.dspark_draft_attention.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp, vp, i64, i32, i32, i32, i32, i32,
                                            ctypes.c_float, i64, vp, vp, i64, vp, vp]
     lib.dspark_draft_attention.restype = ctypes.c_int
+    lib.dspark_pack_combine.argtypes = [vp, i64, i64, i64, i32, vp, i32, ctypes.c_float, vp, ctypes.POINTER(vp)]
+    lib.dspark_pack_combine.restype = ctypes.c_int
+    lib.dspark_combine_hidden_states.argtypes = [vp, vp, i64, i64, vp, i64, vp]
+    lib.dspark_combine_hidden_states.restype = ctypes.c_int
+    lib.dspark_combine_get_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.dspark_combine_get_status.restype = ctypes.c_int
+    lib.dspark_free_combine.argtypes = [vp]
+    lib.dspark_free_combine.restype = None
     lib.dspark_status_string.argtypes = [ctypes.c_int]
     lib.dspark_status_string.restype = ctypes.c_char_p
     _lib = lib

@@ -40,6 +40,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+int device_sm_count(int device) {
+  static int cache[64] = {0};
+  int d = device & 63;
+  if (cache[d] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+    cache[d] = n;
+  }
+  return cache[d];
+}
+
+}  // namespace
+
 // 2-D K-major operand map: rows of `cols` 16-bit elements, `pitch_elems`
 // apart; boxes of kTileK x box_rows with the 128-byte swizzle; out-of-range
 // rows/columns read as zero.
@@ -60,18 +73,6 @@ bool make_operand_map(CUtensorMap* map, const void* base, int dtype, uint64_t co
   return r == CUDA_SUCCESS;
 }
 
-int device_sm_count(int device) {
-  static int cache[64] = {0};
-  int d = device & 63;
-  if (cache[d] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
-    cache[d] = n;
-  }
-  return cache[d];
-}
-
-}  // namespace
 }  // namespace dspark
 
 using namespace dspark;

@@ -67,6 +67,7 @@ struct SmemBarriers {
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
+  float ss_x[kTileM];   // plain mode: the second group's row sums of squares
   uint32_t tmem_base;
   int abort;
   int last_arrival;   // set by the epilogue leader when this CTA finishes a cut tile
@@ -294,6 +295,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   } else {
     regs_increase<kRegsEpilogue>();
     // ------------------------------------------------------------ epilogue
+    // D == 0: plain product mode (main_proj of combine_hidden_states): the
+    // tile is stored in the model dtype with per-row sums of squares of the
+    // stored values; no tokens, pools or heads are involved
+    constexpr bool kPlain = D == 0;
     constexpr int kHalf = D / 2;
     // cos/sin staging for the last item: measured to pay off for D = 128 only
     constexpr bool kStageCs = D == 128;
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const int64_t t = row0 + row;
       bool write = false;
       int64_t loc = 0, pos = 0;
-      if (t < p.T) {
+      if (!kPlain && t < p.T) {
         loc = p.cache_loc[t];
         write = loc >= 0;
         if (write && p.loc_row_width > 0) {
@@ -390,9 +395,11 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // that the row-per-thread reads below are free of bank conflicts): the
       // rotation then reads shared memory instead of waiting on L2 per chunk.
       bool tile_has_k = false;
-      for (int seg = 0; seg < kTileN / D; ++seg) {
-        const int c0 = n_blk * kTileN + seg * D;
-        if (c0 < p.N && c0 % (2 * p.KV) < p.KV) tile_has_k = true;
+      if constexpr (!kPlain) {
+        for (int seg = 0; seg < kTileN / D; ++seg) {
+          const int c0 = n_blk * kTileN + seg * D;
+          if (c0 < p.N && c0 % (2 * p.KV) < p.KV) tile_has_k = true;
+        }
       }
       const bool cs_stage = kStageCs && final_item && tile_has_k;
       auto stage_cs = [&]() {
@@ -561,7 +568,46 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         named_barrier(1, kEpiThreads);   // both halves of every row have landed
       }
       if (tr != nullptr && finish) tr[4] = global_timer_ns();
-      if (finish) {
+      if constexpr (kPlain) {
+        if (finish) {
+          // this group's 128 columns of the row: stored rounded to the model
+          // dtype; the sum of squares is taken over the stored values
+          const int col0 = n_blk * kTileN + group * (kTileN / 2);
+          float ss = 0.f;
+#pragma unroll 1
+          for (int ch = 0; ch < kChunks / 2; ch += 2) {
+            uint32_t v[32], u[32];
+            tmem_ld32x2(t_row + (ch_lo + ch) * 32, t_row + (ch_lo + ch + 1) * 32, v, u);
+            if (t < p.T) {
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint32_t* src = half == 0 ? v : u;
+                const int c = col0 + (ch + half) * 32;
+                if (c >= p.N) continue;
+                E* dst = reinterpret_cast<E*>(p.y) + t * p.y_stride + c;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  uint32_t w[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    w[e] = ElemOps<E>::pack(f32(src[8 * q + 2 * e]), f32(src[8 * q + 2 * e + 1]));
+                    float lo, hi;
+                    ElemOps<E>::unpack(w[e], lo, hi);
+                    ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                  }
+                  st16(dst + 8 * q, w[0], w[1], w[2], w[3]);
+                }
+              }
+            }
+            __syncwarp();
+          }
+          // the two groups' halves of the row, added in a fixed order
+          if (group == 1) bars->ss_x[row] = ss;
+          named_barrier(1, kEpiThreads);
+          if (group == 0 && t < p.T) p.rowsq[t * p.rowsq_stride + n_blk] = ss + bars->ss_x[row];
+          named_barrier(1, kEpiThreads);
+        }
+      } else if (finish) {
 #pragma unroll 1
         for (int seg = group; seg < kTileN / D; seg += 2) {
           const int c0 = n_blk * kTileN + seg * D;
@@ -791,8 +837,17 @@ cudaError_t dispatch(int device, int dtype, int head_dim, bool has_bias, const C
   if (head_dim == 128)
     return has_bias ? launch_one<__half, 128, true, kPair>(device, tx, tw, p, grid, stream)
                     : launch_one<__half, 128, false, kPair>(device, tx, tw, p, grid, stream);
-  return has_bias ? launch_one<__half, 64, true, kPair>(device, tx, tw, p, grid, stream)
-                  : launch_one<__half, 64, false, kPair>(device, tx, tw, p, grid, stream);
+  if (head_dim == 64)
+    return has_bias ? launch_one<__half, 64, true, kPair>(device, tx, tw, p, grid, stream)
+                    : launch_one<__half, 64, false, kPair>(device, tx, tw, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+template <bool kPair>
+cudaError_t dispatch_plain(int device, int dtype, const CUtensorMap& tx, const CUtensorMap& tw,
+                           const WriteParams& p, int grid, cudaStream_t stream) {
+  return dtype == DSPARK_DTYPE_BF16 ? launch_one<__nv_bfloat16, 0, false, kPair>(device, tx, tw, p, grid, stream)
+                                    : launch_one<__half, 0, false, kPair>(device, tx, tw, p, grid, stream);
 }
 
 }  // namespace
@@ -805,6 +860,12 @@ cudaError_t launch_tiled(int device, int dtype, int head_dim, bool has_bias, con
                          const CUtensorMap& tw, const WriteParams& p, int grid,
                          cudaStream_t stream) {
   return dispatch<false>(device, dtype, head_dim, has_bias, tx, tw, p, grid, stream);
+}
+
+cudaError_t launch_plain(int device, int dtype, const CUtensorMap& tx, const CUtensorMap& tw, const WriteParams& p,
+                         int grid, bool pair, cudaStream_t stream) {
+  return pair ? dispatch_plain<true>(device, dtype, tx, tw, p, grid, stream)
+              : dispatch_plain<false>(device, dtype, tx, tw, p, grid, stream);
 }
 
 cudaError_t launch_pair(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tx,

@@ -12,6 +12,12 @@ namespace dspark {
 struct WriteParams {
   int32_t T, H, N, L, NH, D, KV;
   int32_t num_m, num_n, num_kb, num_tiles;
+  // plain product mode (head_dim 0): output [T, N] rows y_stride apart in the
+  // model dtype, and rowsq [T][rowsq_stride] fp32 sums of squares per N tile
+  void* y;
+  int64_t y_stride;
+  float* rowsq;
+  int32_t rowsq_stride;
   const int64_t* positions;
   const int64_t* cache_loc;
   const int32_t* commit_lens;   // null unless window mode
@@ -100,6 +106,18 @@ cudaError_t launch_stream(int device, int dtype, int head_dim, bool has_bias, co
                           const CUtensorMap& tmap_w_half, const WriteParams& p, int t_pad, int stages,
                           uint32_t stage_b, uint32_t acc_stride, uint32_t tmem_cols, int grid,
                           cudaStream_t stream);
+
+// The same kernels in plain product mode: y[T, N] = x[T, K] . w[N, K]^T stored
+// in the model dtype (p.y), with fp32 row sums of squares per 256-column tile
+// (p.rowsq); tiles as launch_tiled (pair = false) or launch_pair.
+cudaError_t launch_plain(int device, int dtype, const CUtensorMap& tmap_x, const CUtensorMap& tmap_w,
+                         const WriteParams& p, int grid, bool pair, cudaStream_t stream);
+
+// 2-D K-major operand map (api.cu): rows of `cols` 16-bit elements,
+// `pitch_elems` apart; boxes of kTileK x box_rows with the 128-byte swizzle;
+// out-of-range rows/columns read as zero.  False if the driver refuses it.
+bool make_operand_map(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint64_t rows,
+                      uint64_t pitch_elems, uint32_t box_rows);
 
 // Number of CTA pairs that can be resident at once on `device` (0 if unknown).
 int pair_workers(int device);

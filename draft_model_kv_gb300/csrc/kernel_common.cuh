@@ -26,6 +26,12 @@ struct ElemOps<__nv_bfloat16> {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
   }
   __device__ static __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+  __device__ static __forceinline__ void unpack(uint32_t u, float& lo, float& hi) {
+    __nv_bfloat162 h;
+    memcpy(&h, &u, 4);
+    lo = __low2float(h);
+    hi = __high2float(h);
+  }
 };
 
 template <>
@@ -39,6 +45,12 @@ struct ElemOps<__half> {
     return __half2float(reinterpret_cast<const __half*>(p)[i]);
   }
   __device__ static __forceinline__ float to_float(__half v) { return __half2float(v); }
+  __device__ static __forceinline__ void unpack(uint32_t u, float& lo, float& hi) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    lo = __low2float(h);
+    hi = __high2float(h);
+  }
 };
 
 __device__ __forceinline__ void flag(const WriteParams& p, uint32_t bits) {

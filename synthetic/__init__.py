@@ -351,3 +351,33 @@ def make_attention_workload(batch: int, block: int, num_q_heads: int, num_kv_hea
                         k_ext=draw(rows, num_kv_heads, D), v_ext=draw(rows, num_kv_heads, D),
                         k_pool=draw(slots, num_kv_heads, D), v_pool=draw(slots, num_kv_heads, D),
                         kv_indices=idx, kv_start=start, sm_scale=float(D) ** -0.5)
+
+
+@dataclasses.dataclass
+class CombineWorkload:
+    """Inputs of combine_hidden_states (bit patterns in ``dtype``)."""
+    dtype: str
+    T: int
+    hidden: int
+    n_aux: int
+    aux: np.ndarray          # [T, n_aux * hidden]
+    weight: np.ndarray       # [hidden, n_aux * hidden]
+    norm_weight: np.ndarray  # [hidden]
+    eps: float
+
+
+def make_combine_workload(name: str = "decode512", tokens: Optional[int] = None, n_aux: int = 3,
+                          hidden: Optional[int] = None, seed: Optional[int] = None) -> CombineWorkload:
+    """The draft model's main_proj / main_norm inputs for a workload's shapes:
+    n_aux auxiliary hidden states of the target, each N(0,1); main_proj
+    weight std (n_aux * hidden)**-0.5; norm weight 1 + 0.1 N(0,1)."""
+    w = make_workload(name, seed, **({} if tokens is None else {"tokens": tokens}))
+    H = w.H if hidden is None else hidden
+    rng = np.random.default_rng(w.seed + 2000)
+    K = n_aux * H
+    return CombineWorkload(dtype=w.dtype, T=w.T, hidden=H, n_aux=n_aux,
+                           aux=to_bits(rng.standard_normal((w.T, K), dtype=np.float32), w.dtype),
+                           weight=to_bits(rng.standard_normal((H, K), dtype=np.float32) * np.float32(K ** -0.5),
+                                          w.dtype),
+                           norm_weight=to_bits(1.0 + 0.1 * rng.standard_normal(H, dtype=np.float32), w.dtype),
+                           eps=w.eps)

@@ -227,3 +227,23 @@ def test_draft_attention_sizes_and_refusals_need_no_gpu(lib):
     assert call(stride=1028) == "E_ALIGNMENT"
     assert call(q=p + 4) == "E_ALIGNMENT"
     assert call(wsb=16) == "E_SCRATCH_LIMIT"
+
+
+def test_combine_refuses_bad_arguments_before_any_gpu_work(lib):
+    buf = ctypes.create_string_buffer(64)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16
+    out = ctypes.c_void_p()
+    f = lib.dspark_pack_combine
+
+    def pack(w=p, H=4096, K=12288, stride=12288, dtype=1, nw=p, ndt=3, eps=1e-6):
+        return _abi.STATUS[f(w, H, K, stride, dtype, nw, ndt, eps, None, ctypes.byref(out))]
+
+    assert pack(w=None) == "E_INVALID_ARG"
+    assert pack(dtype=3) == "E_DTYPE_MISMATCH"
+    assert pack(ndt=9) == "E_DTYPE_MISMATCH"
+    assert pack(H=4016) == "E_SHAPE_MISMATCH"       # not a multiple of 32
+    assert pack(stride=100) == "E_SHAPE_MISMATCH"
+    assert pack(w=p + 2) == "E_ALIGNMENT"
+    assert pack(eps=-1.0) == "E_INVALID_ARG"
+    assert _abi.STATUS[lib.dspark_combine_hidden_states(None, p, 4, 8, p, 8, None)] == "E_INVALID_ARG"
+    lib.dspark_free_combine(None)

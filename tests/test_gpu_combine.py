@@ -1,0 +1,73 @@
+"""Parity of combine_hidden_states (main_proj on the tcgen05 kernel in plain
+mode, then the in-place norm) with its oracle, within the model dtype's
+tolerance (bf16 2e-2, fp16 5e-3, rtol = atol; the outputs are normalised to
+unit mean square), on the context-KV workloads' shapes."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from synthetic.device import bits_to_tensor
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from draft_model_kv_gb300 import build
+    build.build()
+
+
+def run(cw, pad=0):
+    import draft_model_kv_gb300 as dk
+    dt = torch.bfloat16 if cw.dtype == "bf16" else torch.float16
+    W = bits_to_tensor(cw.weight, dt, "cuda")
+    c = dk.dspark_pack_combine(W, bits_to_tensor(cw.norm_weight, dt, "cuda"), cw.eps)
+    aux = bits_to_tensor(cw.aux, dt, "cuda")
+    out = torch.full((cw.T, cw.hidden + pad), 7.0, dtype=dt, device="cuda")
+    dk.dspark_combine_hidden_states(c, aux, out=out[:, :cw.hidden])
+    torch.cuda.synchronize()
+    assert dk.dspark_combine_get_status(c) == 0
+    c.free()
+    return out
+
+
+def check(cw, out, rows=None):
+    rows = np.arange(cw.T) if rows is None else np.asarray(rows)
+    ref = oracle.combine_hidden_states(cw.aux[rows], cw.weight, cw.norm_weight, cw.eps, cw.dtype)
+    got = out[torch.from_numpy(rows).cuda(), :cw.hidden].double().cpu().numpy()
+    tol = 2e-2 if cw.dtype == "bf16" else 5e-3
+    np.testing.assert_allclose(got, ref, rtol=tol, atol=tol)
+
+
+@pytest.mark.parametrize("T", [1, 7, 130, 300])
+def test_small_hidden_ragged_tokens(T):
+    cw = synthetic.make_combine_workload("tiny", tokens=T, hidden=512)
+    out = run(cw, pad=8)
+    check(cw, out)
+    np.testing.assert_array_equal(out[:, cw.hidden:].float().cpu().numpy(), 7.0)   # padding untouched
+
+
+def test_decode512_shapes_sampled():
+    cw = synthetic.make_combine_workload("decode512")
+    out = run(cw)
+    rows = np.sort(np.random.default_rng(4).choice(cw.T, size=48, replace=False))
+    check(cw, out, rows=np.concatenate([[0], rows, [cw.T - 1]]))
+
+
+@pytest.mark.parametrize("name,T", [("fp16bias", 64), ("k3gqa", 40)])
+def test_other_shapes(name, T):
+    cw = synthetic.make_combine_workload(name, tokens=T)
+    out = run(cw)
+    check(cw, out)
+
+
+def test_deterministic():
+    cw = synthetic.make_combine_workload("tiny", tokens=200, hidden=1024)
+    a = run(cw)
+    b = run(cw)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
