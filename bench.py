@@ -361,8 +361,8 @@ NCU_TRAFFIC = {
     # (workload, tokens) -> per-launch DRAM bytes (read + write) of the fused
     # kernel from one ncu capture of the kernel as it stands (summaries under
     # profiles/); anything without a capture of the current kernel reports null
-    ("decode512", 512): 91.431424e6 + 8.855552e6,
-    ("decode512", 16): 84.098560e6 + 2.786816e6,
+    ("decode512", 512): 91.499264e6 + 8.760576e6,
+    ("decode512", 16): 84.099584e6 + 2.691840e6,
 }
 
 
@@ -770,7 +770,8 @@ def run_combine(args):
     if rank != 0:
         return None
     tensor = {"bound": "tensor", "achieved": flops / t_step / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-              "frac": flops / t_step / 1e12 / pk["bf16_tflops"], "traffic": None,
+              "frac": flops / t_step / 1e12 / pk["bf16_tflops"],
+              "traffic": COMBINE_NCU_TRAFFIC.get((args.workload, cw.T)),
               "peak_source": pk["source"] + " (burst: the kernel is timed alone)"}
     hbm = {"bound": "hbm", "achieved": bytes_ / t_step / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
            "frac": bytes_ / t_step / 1e9 / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"]}
@@ -803,9 +804,17 @@ def run_combine(args):
     return res
 
 
+COMBINE_NCU_TRAFFIC = {
+    # (workload, tokens) -> per-launch DRAM bytes of the main_proj product
+    # kernel from an ncu capture of the kernel as it stands; null without one
+    ("prefill32k", 4096): 498.602752e6 + 44.845312e6,
+}
+
+
 ATTN_NCU_TRAFFIC = {
     # (requests, total context tokens) -> per-launch DRAM bytes of the split
     # kernel from an ncu capture of the kernel as it stands; null without one
+    (64, 262144): 1082.343e6 + 44.051456e6,
 }
 
 
