@@ -71,3 +71,36 @@ def test_deterministic():
     a = run(cw)
     b = run(cw)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_combine_then_write_matches_the_oracle_pipeline():
+    """The draft step's front half: combine_hidden_states produces ctx_hidden
+    on the device and the context-KV write consumes it.  The oracle side runs
+    the same two steps from the same inputs (its ctx_hidden rounded to the
+    model dtype by the oracle's own rounding), never from device values."""
+    import dataclasses
+    import draft_model_kv_gb300 as dk
+    from synthetic.device import stage
+    w = synthetic.make_workload("decode512", tokens=64)
+    cw = synthetic.make_combine_workload("decode512", tokens=64)
+    # the write's input is the oracle's combine output, in the model dtype
+    ref_hidden = oracle.round_to(oracle.combine_hidden_states(cw.aux, cw.weight, cw.norm_weight, cw.eps,
+                                                              cw.dtype), cw.dtype)
+    w_ref = dataclasses.replace(w, ctx_hidden=synthetic.f32_to_bf16_bits(ref_hidden.astype(np.float32)))
+    ref = oracle.run_workload(w_ref)
+    st = stage(w)
+    dt = torch.bfloat16
+    c = dk.dspark_pack_combine(bits_to_tensor(cw.weight, dt, "cuda"), bits_to_tensor(cw.norm_weight, dt, "cuda"),
+                               cw.eps)
+    hidden = dk.dspark_combine_hidden_states(c, bits_to_tensor(cw.aux, dt, "cuda"))
+    b = dk.dspark_pack_ctx_kv(st["layers"], w.H)
+    dk.dspark_write_ctx_kv(b, hidden, st["positions"], st["cos_sin"], st["cache_loc"], st["k_pools"],
+                           st["v_pools"], commit_lens=st["commit_lens"], loc_row_width=st["loc_row_width"])
+    torch.cuda.synchronize()
+    assert dk.dspark_get_device_status(b) == 0 and dk.dspark_combine_get_status(c) == 0
+    slots = torch.from_numpy(ref.slots).cuda()
+    for l in range(w.L):
+        np.testing.assert_allclose(st["k_pools"][l][slots].double().cpu().numpy(), ref.k[l], rtol=2e-2, atol=2e-2)
+        np.testing.assert_allclose(st["v_pools"][l][slots].double().cpu().numpy(), ref.v[l], rtol=2e-2, atol=2e-2)
+    b.free()
+    c.free()
