@@ -316,8 +316,7 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
     p.num_m = 1;
     p.num_n = static_cast<int32_t>(b->N / 128);
     p.num_tiles = p.num_n;
-    int grid = 0;
-    plan_schedule(p.num_tiles, p.num_kb, b->sms, &grid, &p.dp_tiles, &p.sk_units);
+    const int grid = plan_schedule(p.num_tiles, p.num_kb, b->sms, false, p);
     const cudaError_t e = launch_stream(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w_half, p,
                                         t_pad, stages, stage_b, acc_stride, tmem_cols, grid, stream);
     return e == cudaSuccess ? DSPARK_OK : DSPARK_E_CUDA;
@@ -334,8 +333,7 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   p.num_m = static_cast<int32_t>((T + tile_rows - 1) / tile_rows);
   p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
   p.num_tiles = p.num_m * p.num_n;
-  int workers = 0;
-  plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : b->sms, &workers, &p.dp_tiles, &p.sk_units);
+  const int workers = plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : b->sms, true, p);
   const int grid = pair ? 2 * workers : workers;
   const cudaError_t e =
       pair ? launch_pair(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w_half, p, grid, stream)

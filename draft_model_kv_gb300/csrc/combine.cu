@@ -203,8 +203,7 @@ int dspark_combine_hidden_states(dspark_combine_t c, const void* aux, int64_t T,
   p.y_stride = out_row_stride;
   p.rowsq = c->rowsq;
   p.rowsq_stride = n_tiles;
-  int workers = 0;
-  plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : c->sms, &workers, &p.dp_tiles, &p.sk_units);
+  const int workers = plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : c->sms, true, p);
   cudaError_t e = launch_plain(device, c->dtype, tmap_x, pair ? c->tmap_w_half : c->tmap_w, p,
                                pair ? 2 * workers : workers, pair, stream);
   if (e != cudaSuccess) return DSPARK_E_CUDA;

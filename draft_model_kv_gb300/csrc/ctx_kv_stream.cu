@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       int c_first = 0, c_last = 0;
       if (cut) {
         const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
-        c_first = sk_owner(p, u0, nw);
-        c_last = sk_owner(p, u0 + p.num_kb - 1, nw);
+        c_first = sk_owner(p, u0);
+        c_last = sk_owner(p, u0 + p.num_kb - 1);
       }
       bool early = false;
       float4 pre[8];

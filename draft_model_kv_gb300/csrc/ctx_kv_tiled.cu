@@ -61,13 +61,15 @@ static_assert(kTiledThreads == 384, "three warpgroups");
 static_assert(128 * kRegsControl + 256 * kRegsEpilogue == 384 * kLaunchRegs,
               "the register split must use exactly the launch allocation");
 
+constexpr int kRedBatch = 8;   // parts of a split tile whose loads are in flight together
+
 struct SmemBarriers {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
-  float ss_x[kTileM];   // plain mode: the second group's row sums of squares
+  float ss_x[kTileM];   // plain mode: the second group's row sums of squares; split rows: per-warp sums
   uint32_t tmem_base;
   int abort;
   int last_arrival;   // set by the epilogue leader when this CTA finishes a cut tile
@@ -82,6 +84,220 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   const int r = tile - group * group_size;
   m_blk = first_m + r % gm;
   n_blk = r / gm;
+}
+
+// Whether token t's rows are written, with its pool slot and position (sglang
+// PR #31847 summary page, fused_kv_norm_rope_write: loc < 0 skips the token;
+// in window mode column t mod W must be below commit_lens[t div W]).  Range
+// errors are flagged (by the caller's chosen thread) and skip the token.
+__device__ __forceinline__ bool token_write(const WriteParams& p, int64_t t, bool raise, int64_t& loc,
+                                            int64_t& pos) {
+  loc = 0;
+  pos = 0;
+  if (t >= p.T) return false;
+  loc = p.cache_loc[t];
+  if (loc < 0) return false;
+  if (p.loc_row_width > 0) {
+    const int64_t b = t / p.loc_row_width;
+    if (t - b * p.loc_row_width >= static_cast<int64_t>(p.commit_lens[b])) return false;
+  }
+  pos = p.positions[t];
+  if (pos < 0 || pos >= p.max_pos) {
+    if (raise) flag(p, DSPARK_FLAG_POS_RANGE);
+    return false;
+  }
+  if (loc >= p.pool_slots) {
+    if (raise) flag(p, DSPARK_FLAG_LOC_RANGE);
+    return false;
+  }
+  return true;
+}
+
+// Bounded wait until *ctr >= target (acquire).
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int target, volatile int* abort_flag,
+                                           uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_gpu(ctr) < target) {
+    if (*abort_flag != 0 || global_timer_ns() - t0 > limit_ns) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// The cut tiles of the split-first schedule (the tiles left over after the
+// full wave, whose k-blocks are spread over the workers).  Every contributor
+// publishes its part before any is read; then contributor i of n finishes
+// rows [i*rv/n, (i+1)*rv/n) of its CTA's rows of the tile: it sums them over
+// all n parts in ascending contributor order (so the bits do not depend on
+// arrival order) and runs the epilogue on them -- K RMSNorm and RoPE and the
+// pool scatter, or the plain product's store and row sums of squares.
+//
+// Rows go 8 at a time.  Lane l of a warp takes row l % 8 and, in each of two
+// 16-column blocks of the tile, the float4 column group l / 8: the loads of a
+// warp are four 128-byte runs of the workspace's [column group][row] layout.
+// A warp's two blocks are the two halves' blocks of one rotation pair (block b
+// and b + D/32 of a head), so RoPE stays inside a lane; the warps of a head
+// add their parts of the sum of squares through shared memory.  It runs on the
+// epilogue warps while the CTA's whole tile is on the tensor cores.  Returns
+// false if a wait ran out.
+template <typename E, int D, bool kBias, bool kPair>
+__device__ bool finish_split_rows(const WriteParams& p, int wid, int nw, uint32_t rank, float* ss_part,
+                                  volatile int* abort_flag) {
+  using G = Geo<kPair>;
+  constexpr bool kPlain = D == 0;
+  constexpr int kRows = 8;                                    // rows per pass
+  constexpr int kBH = kPlain ? 2 : D / 16;                    // 16-column blocks per head
+  constexpr int kWPH = kPlain ? 1 : kBH / 2;                  // warps per head
+  const int etid = threadIdx.x, warp = etid / 32, lane = etid % 32;
+  const int rr = lane % kRows, gs = lane / kRows;
+  const int hd = warp / kWPH;                                 // head of the tile (write mode)
+  const int b1 = kPlain ? 2 * warp : kBH * hd + warp % kWPH;  // this warp's two blocks
+  const int b2 = kPlain ? 2 * warp + 1 : b1 + kBH / 2;
+  const int g1 = 4 * b1 + gs, g2 = 4 * b2 + gs;               // float4 column groups of the lane
+  const WorkIter range = work_begin(p, wid, nw);
+  if (range.cur <= range.start) return true;
+  const int64_t t_lo = range.start / p.num_kb, t_hi = (range.cur - 1) / p.num_kb;
+  auto cta_of = [&](int c) { return kPair ? 2 * c + static_cast<int>(rank) : c; };
+  for (int64_t st = t_lo; st <= t_hi; ++st) {
+    const int64_t u0 = st * p.num_kb;
+    const int cf = sk_owner(p, u0), cl = sk_owner(p, u0 + p.num_kb - 1);
+    if (cf == cl) continue;   // a whole tile: finished from TMEM
+    const int n = cl - cf + 1;
+    int32_t* counter = p.counters + cta_of(cl);
+    bool ok = true;
+    if (etid == 0) {
+      ok = wait_count(counter, n, abort_flag, p.wait_limit_ns);
+      // second round: the last contributor past the wait resets the counter
+      // for the next launch (every contributor has already read it as n)
+      if (ok && atom_add_acq_rel_gpu(counter, 1) == 2 * n - 1) *counter = 0;
+    }
+    if (!named_barrier_and(1, kEpiThreads, ok)) return false;
+    int m_blk, n_blk;
+    tile_coords(p.dp_tiles + static_cast<int>(st), p.num_m, p.num_n, m_blk, n_blk);
+    const int64_t row0 = static_cast<int64_t>(m_blk) * G::kTileRows + static_cast<int64_t>(rank) * kTileM;
+    const int64_t left = static_cast<int64_t>(p.T) - row0;
+    const int rv = left <= 0 ? 0 : (left < kTileM ? static_cast<int>(left) : kTileM);
+    const int i = wid - cf;
+    const int lo = i * rv / n, hi = (i + 1) * rv / n;
+#pragma unroll 1
+    for (int r0 = lo; r0 < hi; r0 += kRows) {
+      const int row = r0 + rr;
+      const bool valid = row < hi;
+      float4 s1 = make_float4(0.f, 0.f, 0.f, 0.f), s2 = s1;
+#pragma unroll 1
+      for (int c = cf; c <= cl; c += kRedBatch) {
+        float4 q1[kRedBatch], q2[kRedBatch];
+#pragma unroll
+        for (int j = 0; j < kRedBatch; ++j) {
+          q1[j] = q2[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (valid && c + j <= cl) {
+            const float4* src = reinterpret_cast<const float4*>(ws_slot(p, cta_of(c + j), c + j == cf ? 1 : 0));
+            q1[j] = __ldcg(src + g1 * kTileM + row);
+            q2[j] = __ldcg(src + g2 * kTileM + row);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kRedBatch; ++j) {
+          if (c + j <= cl) {
+            s1 = c + j == cf ? q1[j] : add4(s1, q1[j]);
+            s2 = c + j == cf ? q2[j] : add4(s2, q2[j]);
+          }
+        }
+      }
+      const int64_t t = row0 + row;
+      if constexpr (kPlain) {
+        // stored rounded to the model dtype; the sum of squares is taken over
+        // the stored values
+        const float4 sv[2] = {s1, s2};
+        const int gg[2] = {g1, g2};
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t w0 = ElemOps<E>::pack(sv[k].x, sv[k].y), w1 = ElemOps<E>::pack(sv[k].z, sv[k].w);
+          float a, b, c2, d;
+          ElemOps<E>::unpack(w0, a, b);
+          ElemOps<E>::unpack(w1, c2, d);
+          const int col = n_blk * kTileN + 4 * gg[k];
+          if (col < p.N) {
+            ss = fmaf(a, a, fmaf(b, b, fmaf(c2, c2, fmaf(d, d, ss))));
+            if (valid)
+              *reinterpret_cast<uint2*>(reinterpret_cast<E*>(p.y) + t * p.y_stride + col) = make_uint2(w0, w1);
+          }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+        if (gs == 0) ss_part[warp * kRows + rr] = ss;
+        named_barrier(1, kEpiThreads);
+        if (warp == 0 && lane < kRows && r0 + lane < hi) {
+          float tot = 0.f;
+#pragma unroll
+          for (int w = 0; w < kEpiWarps; ++w) tot += ss_part[w * kRows + lane];
+          p.rowsq[(row0 + r0 + lane) * p.rowsq_stride + n_blk] = tot;
+        }
+      } else {
+        constexpr int kHalf = D / 2;
+        const int i1 = 4 * g1 - hd * D;   // column inside the head (first half); partner i1 + D/2
+        const int c0 = n_blk * kTileN + hd * D;
+        const bool col_ok = c0 < p.N;
+        int64_t loc = 0, pos = 0;
+        const bool write = valid && col_ok && token_write(p, t, warp == 0 && gs == 0, loc, pos);
+        const int cv = col_ok ? c0 : 0;
+        const int layer = cv / (2 * p.KV);
+        const int r = cv - layer * 2 * p.KV;
+        const bool is_v = r >= p.KV;
+        const int head = (is_v ? r - p.KV : r) / D;
+        float x1[4] = {s1.x, s1.y, s1.z, s1.w}, x2[4] = {s2.x, s2.y, s2.z, s2.w};
+        if (kBias && col_ok) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x1[e] += ElemOps<E>::load(p.bias, c0 + i1 + e);
+            x2[e] += ElemOps<E>::load(p.bias, c0 + kHalf + i1 + e);
+          }
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ss = fmaf(x1[e], x1[e], fmaf(x2[e], x2[e], ss));
+        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+        if (gs == 0) ss_part[warp * kRows + rr] = ss;
+        named_barrier(1, kEpiThreads);
+        if (!is_v) {
+          float tot = 0.f;
+#pragma unroll
+          for (int k = 0; k < kWPH; ++k) tot += ss_part[(hd * kWPH + k) * kRows + rr];
+          const float inv = rsqrtf(tot * (1.0f / D) + p.eps);
+          const float* w = p.knorm + static_cast<int64_t>(layer) * D;
+          const float4 w1 = *reinterpret_cast<const float4*>(w + i1);
+          const float4 w2 = *reinterpret_cast<const float4*>(w + kHalf + i1);
+          const float* cs = p.cos_sin + (write ? pos : 0) * D;
+          const float4 c4 = *reinterpret_cast<const float4*>(cs + i1);
+          const float4 s4 = *reinterpret_cast<const float4*>(cs + kHalf + i1);
+          const float wa[4] = {w1.x, w1.y, w1.z, w1.w}, wb[4] = {w2.x, w2.y, w2.z, w2.w};
+          const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = x1[e] * inv * wa[e];
+            const float b = x2[e] * inv * wb[e];
+            x1[e] = a * cc[e] - b * sn[e];
+            x2[e] = b * cc[e] + a * sn[e];
+          }
+        }
+        if (write) {
+          E* dst = is_v ? reinterpret_cast<E*>(p.v_pool[layer]) + loc * p.v_stride[layer] + head * D
+                        : reinterpret_cast<E*>(p.k_pool[layer]) + loc * p.k_stride[layer] + head * D;
+          *reinterpret_cast<uint2*>(dst + i1) = make_uint2(ElemOps<E>::pack(x1[0], x1[1]), ElemOps<E>::pack(x1[2], x1[3]));
+          *reinterpret_cast<uint2*>(dst + kHalf + i1) =
+              make_uint2(ElemOps<E>::pack(x2[0], x2[1]), ElemOps<E>::pack(x2[2], x2[3]));
+        }
+      }
+      named_barrier(1, kEpiThreads);   // ss_part is rewritten by the next pass
+    }
+  }
+  return true;
 }
 
 template <typename E, int D, bool kBias, bool kPair>
@@ -319,6 +535,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     while (work_next(p, it, tile, kb0, kb1)) {
       int m_blk, n_blk;
       tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+      // split-first schedule: after the last part of the stream-K range is
+      // published, finish this worker's share of its cut tiles
+      const bool reduce_after = p.sk_first && tile >= p.dp_tiles && it.cur <= it.start;
       bool final_item;
       {
         WorkIter peek = it;
@@ -329,26 +548,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // depend on the accumulator, so it runs while the MMAs are in flight
       const int64_t row0 = static_cast<int64_t>(m_blk) * G::kTileRows + static_cast<int64_t>(rank) * kTileM;
       const int64_t t = row0 + row;
-      bool write = false;
       int64_t loc = 0, pos = 0;
-      if (!kPlain && t < p.T) {
-        loc = p.cache_loc[t];
-        write = loc >= 0;
-        if (write && p.loc_row_width > 0) {
-          const int64_t b = t / p.loc_row_width;
-          if (t - b * p.loc_row_width >= static_cast<int64_t>(p.commit_lens[b])) write = false;
-        }
-        if (write) {
-          pos = p.positions[t];
-          if (pos < 0 || pos >= p.max_pos) {
-            if (group == 0) flag(p, DSPARK_FLAG_POS_RANGE);
-            write = false;
-          } else if (loc >= p.pool_slots) {
-            if (group == 0) flag(p, DSPARK_FLAG_LOC_RANGE);
-            write = false;
-          }
-        }
-      }
+      const bool write = !kPlain && token_write(p, t, group == 0, loc, pos);
       if (write) {
         // the K heads of this tile will read this token's cos/sin row
         const char* cs_row = reinterpret_cast<const char*>(p.cos_sin + pos * D);
@@ -360,7 +561,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const bool cut = kb0 != 0 || kb1 != p.num_kb;
       if (cut && final_item && etid == 0) {
         const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
-        const int cf = sk_owner(p, u0, nw), cl = sk_owner(p, u0 + p.num_kb - 1, nw);
+        const int cf = sk_owner(p, u0), cl = sk_owner(p, u0 + p.num_kb - 1);
         const int seen = ld_acquire_gpu(p.counters + (kPair ? 2 * cl + static_cast<int>(rank) : cl));
         *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == cl - cf;
       }
@@ -419,8 +620,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
         // contributors are workers (CTAs, or CTA pairs whose halves are
         // finished independently: the slot and counter of a pair CTA carry its rank)
-        const int c_first = sk_owner(p, u0, nw);
-        const int c_last = sk_owner(p, u0 + p.num_kb - 1, nw);
+        const int c_first = sk_owner(p, u0);
+        const int c_last = sk_owner(p, u0 + p.num_kb - 1);
         const int me = wid;
         auto cta_of = [&](int c) { return kPair ? 2 * c + static_cast<int>(rank) : c; };
         int32_t* counter = p.counters + cta_of(c_last);
@@ -463,7 +664,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           named_barrier(1, kEpiThreads);                  // every row of the part is written
           if (etid == 0) {
             const int old = atom_add_acq_rel_gpu(counter, 1);
-            const int last = old == c_last - c_first;
+            // (split-first: every contributor finishes a share of the rows instead)
+            const int last = !p.sk_first && old == c_last - c_first;
             if (last) *counter = 0;   // ready for the next launch
             *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
           }
@@ -756,6 +958,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+      if (reduce_after) {
+        if (!finish_split_rows<E, D, kBias, kPair>(p, wid, nw, rank, bars->ss_x, abort_flag)) {
+          if (etid == 0) {
+            *abort_flag = 1;
+            flag(p, DSPARK_FLAG_TIMEOUT);
+          }
+          break;
+        }
+        if (trace != nullptr && etid == 0) trace[kTraceWords - 1] = global_timer_ns();   // split rows done
       }
     }
   }

@@ -80,31 +80,35 @@ __device__ __forceinline__ void st16(void* dst, uint32_t a, uint32_t b, uint32_t
   *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
 }
 
-// Work of one CTA: first its whole tiles of the data-parallel waves, then its
-// contiguous range of the stream-K k-block space, walked from its end back to
-// its start.  The backward walk makes a CTA begin with the (usually small)
-// first k-blocks of the tile at the end of its range, publish that part while
-// it computes the rest, and end with the (usually large) last part of the tile
-// at the start of its range, which it then finishes itself: the partial tile
-// it holds in TMEM is the last to arrive.
+// Work of one worker (a CTA, or a CTA pair): its whole tiles (every nw-th
+// from its index) and its contiguous range of the stream-K k-block space,
+// walked from its end back to its start; whole tiles first unless the
+// schedule is split-first.  In the other order the backward walk makes a
+// worker begin with the (usually small) first k-blocks of the tile at the end
+// of its range, publish that part while it computes the rest, and end with
+// the (usually large) last part of the tile at the start of its range, which
+// it then finishes itself: the partial tile it holds in TMEM is the last to
+// arrive.
 struct WorkIter {
   int dp_tile, nw;
   int64_t start, cur;
 };
 
-// `wid` of `nw` workers: a CTA, or a CTA pair.
 __device__ __forceinline__ WorkIter work_begin(const WriteParams& p, int wid, int nw) {
   WorkIter it;
   it.dp_tile = wid;
   it.nw = nw;
-  it.start = static_cast<int64_t>(wid) * p.sk_units / nw;
-  it.cur = static_cast<int64_t>(wid + 1) * p.sk_units / nw;
+  it.start = it.cur = 0;
+  if (wid < p.sk_workers) {
+    it.start = static_cast<int64_t>(wid) * p.sk_units / p.sk_workers;
+    it.cur = static_cast<int64_t>(wid + 1) * p.sk_units / p.sk_workers;
+  }
   return it;
 }
 
 __device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, int& tile, int& kb0,
                                           int& kb1) {
-  if (it.dp_tile < p.dp_tiles) {
+  if (!p.sk_first && it.dp_tile < p.dp_tiles) {
     tile = it.dp_tile;
     kb0 = 0;
     kb1 = p.num_kb;
@@ -121,12 +125,19 @@ __device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, in
     tile = p.dp_tiles + static_cast<int>(t);
     return true;
   }
+  if (p.sk_first && it.dp_tile < p.dp_tiles) {
+    tile = it.dp_tile;
+    kb0 = 0;
+    kb1 = p.num_kb;
+    it.dp_tile += it.nw;
+    return true;
+  }
   return false;
 }
 
 // Worker whose stream-K range holds k-block unit u.
-__device__ __forceinline__ int sk_owner(const WriteParams& p, int64_t u, int nw) {
-  return static_cast<int>(((u + 1) * nw - 1) / p.sk_units);
+__device__ __forceinline__ int sk_owner(const WriteParams& p, int64_t u) {
+  return static_cast<int>(((u + 1) * p.sk_workers - 1) / p.sk_units);
 }
 
 // Partial-tile slot of a CTA: [kTileN/4][kTileM] float4, so that the 32 rows

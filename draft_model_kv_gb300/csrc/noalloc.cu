@@ -176,8 +176,7 @@ extern "C" int dspark_write_ctx_kv_noalloc(
   p.num_kb = (hidden + kTileK - 1) / kTileK;
   p.num_tiles = p.num_m * p.num_n;
   const int ctas = scratch->sms < kNoAllocMaxCtas ? scratch->sms : kNoAllocMaxCtas;
-  int grid = 0;
-  plan_schedule(p.num_tiles, p.num_kb, ctas, &grid, &p.dp_tiles, &p.sk_units);
+  const int grid = plan_schedule(p.num_tiles, p.num_kb, ctas, true, p);
   // the workspace this launch uses must fit in the static array
   if (workspace_bytes(grid) > kNoAllocWorkspaceBytes || grid > kNoAllocMaxCtas)
     return DSPARK_E_SCRATCH_LIMIT;

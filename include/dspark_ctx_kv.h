@@ -252,7 +252,8 @@ DSPARK_API int dspark_set_kernel_variant(dspark_bundle_t bundle, int32_t variant
 /* Diagnostics: make later writes with this bundle record a per-CTA timeline
  * into `buf` (device, uint64 [SMs x 64]: globaltimer ns at CTA start and end,
  * the number of work items, then per work item its tile, its k-block range and
- * kind, and the times its accumulator became ready and was released).  `words`
+ * kind, and the times its accumulator became ready and was released; the last
+ * word: when the CTA finished its rows of the leftover split tiles).  `words`
  * is the buffer length; NULL turns tracing off (the default).  Tracing adds a
  * few global stores per work item and does not change results. */
 DSPARK_API int dspark_set_trace_buffer(dspark_bundle_t bundle, uint64_t* buf, int64_t words);

@@ -66,6 +66,16 @@ def test_other_shapes(name, T):
     check(cw, out)
 
 
+def test_one_wave_of_tiles():
+    # 94 tiles of 256 x 256 on 76 CTA pairs: the leftover tiles are split over
+    # every pair and each contributor stores its share of their rows
+    cw = synthetic.make_combine_workload("tiny", tokens=12000, hidden=512)
+    out = run(cw)
+    check(cw, out)
+    again = run(cw)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
 def test_deterministic():
     cw = synthetic.make_combine_workload("tiny", tokens=200, hidden=1024)
     a = run(cw)

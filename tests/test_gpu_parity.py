@@ -215,6 +215,33 @@ def test_k3gqa_sampled():
     check_values(w, st, sample=edge_sample(w.T))
 
 
+# ------------------------------------------------------------------ one-wave problems
+
+@pytest.mark.parametrize("variant", ["single", "pair"])
+@pytest.mark.parametrize("name,kw", [("decode512", ()), ("fp16bias", (("tokens", 304),)),
+                                     ("k3gqa", (("tokens", 1000),)), ("tiny", (("tokens", 12000),)),
+                                     ("tiny", (("tokens", 12000), ("H", 64)))])
+def test_one_wave_problems(name, kw, variant):
+    """Between one and two waves of tiles: the leftover tiles' k-blocks are
+    spread over every worker and each contributor finishes a share of their
+    rows (bias, head_dim 64, a ragged last token block, and with H = 64 a
+    single k-block per tile, where no tile is cut at all)."""
+    w = workload(name, **dict(kw))
+    st, _, flags = run_gpu(w, variant=variant)
+    assert flags == 0
+    check_placement(w, st)
+    check_values(w, st)
+
+
+@pytest.mark.parametrize("variant", ["single", "pair"])
+def test_one_wave_repeat_is_bitwise_deterministic(variant):
+    w = workload("k3gqa", tokens=1000)
+    st1, _, _ = run_gpu(w, variant=variant)
+    st2, _, _ = run_gpu(w, variant=variant)
+    for a, b in zip(st1["k_pools"] + st1["v_pools"], st2["k_pools"] + st2["v_pools"]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 # ------------------------------------------------------------------ edge cases and errors
 
 def test_zero_tokens_is_a_noop():
