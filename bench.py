@@ -361,7 +361,7 @@ NCU_TRAFFIC = {
     # (workload, tokens) -> per-launch DRAM bytes (read + write) of the fused
     # kernel from one ncu capture of the kernel as it stands (summaries under
     # profiles/); anything without a capture of the current kernel reports null
-    ("decode512", 512): 90.166016e6 + 10.643200e6,
+    ("decode512", 512): 90.609664e6 + 12.175360e6,
     ("decode512", 16): 84.097024e6 + 2.508800e6,
 }
 
@@ -807,7 +807,7 @@ def run_combine(args):
 COMBINE_NCU_TRAFFIC = {
     # (workload, tokens) -> per-launch DRAM bytes of the main_proj product
     # kernel from an ncu capture of the kernel as it stands; null without one
-    ("prefill32k", 4096): 498.602752e6 + 44.845312e6,
+    ("prefill32k", 4096): 488.811008e6 + 43.305728e6,
 }
 
 

@@ -11,7 +11,8 @@
 //               (tcgen05.ld 32x32b), so the RMSNorm sum of squares is a
 //               per-thread sum and the neox pair (i, i + D/2) sits in the same
 //               thread's registers; then 16-byte stores into the pool row
-//   warp 8      TMA producer: X and W_all K-slices into a 4-stage smem ring
+//   warp 8      TMA producer: X and W_all K-slices into a smem ring (4 stages,
+//               or 5 for CTA pairs)
 //   warp 9      MMA issuer: tcgen05.mma 128x256x16 into one of two TMEM
 //               accumulators (2 x 256 fp32 columns); owns TMEM alloc/free
 //   warps 10,11 idle (they complete the control warpgroup)
@@ -36,19 +37,20 @@ namespace {
 // Operand staging of one CTA.  Single-CTA tiles are 128 tokens x 256 columns;
 // pair tiles are 256 tokens x 256 columns computed by two CTAs of a cluster
 // with tcgen05.mma.cta_group::2: each CTA holds its 128 token rows of X and
-// half (128 rows) of the W tile, so a stage is 32 KB and six fit in the ring.
+// half (128 rows) of the W tile, so a stage is 32 KB; five of them (160 KB)
+// measured faster than six on the large workloads (a smaller shared-memory
+// carve-out leaves more L1), and no slower at 512 tokens.
 template <bool kPair>
 struct Geo {
   static constexpr int kTileRows = kPair ? 2 * kTileM : kTileM;   // token rows of a work tile
   static constexpr int kBRows = kPair ? kTileN / 2 : kTileN;       // W rows per CTA per stage
   static constexpr uint32_t kStageA = kTileM * kTileK * 2;         // 16 KB
   static constexpr uint32_t kStageB = kBRows * kTileK * 2;         // 16 KB (pair) or 32 KB
-  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kStages = kPair ? 5 : 4;
   static constexpr uint32_t kRingBytes = kStages * (kStageA + kStageB);
 };
-constexpr int kMaxStages = 6;
-constexpr uint32_t kRingBytes = Geo<false>::kRingBytes;
-static_assert(Geo<true>::kRingBytes == kRingBytes, "both layouts use the same ring");
+constexpr int kMaxStages = 5;
+static_assert(Geo<false>::kStages <= kMaxStages && Geo<true>::kStages <= kMaxStages, "barrier arrays");
 constexpr uint32_t kAccCols = kTileN;                    // fp32 columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;             // double buffer = 512 (all of TMEM)
 constexpr int kEpiWarps = 8;                             // two epilogue warpgroups
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* smem_a = smem;
   uint8_t* smem_b = smem + kStages * kStageBytesA;
-  SmemBarriers* bars = reinterpret_cast<SmemBarriers*>(smem + kRingBytes);
+  SmemBarriers* bars = reinterpret_cast<SmemBarriers*>(smem + G::kRingBytes);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     // cos/sin staging for the last item: measured to pay off for D = 128 only
     constexpr bool kStageCs = D == 128;
     constexpr uint32_t kCsBytes = kStageCs ? kTileM * D * 4 : 0;
-    static_assert(kCsBytes <= kRingBytes / 2, "cos/sin staging leaves room for the fixup");
+    static_assert(kCsBytes <= G::kRingBytes / 2, "cos/sin staging leaves room for the fixup");
     constexpr int kChunks = kTileN / 32;            // 32-column chunks of a tile
     const int group = warp / 4;                     // warpgroup 0 or 1
     const int quarter = warp % 4;                   // TMEM lanes this warp may read
@@ -691,7 +693,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           // are staged there (each group in its own half) with many asynchronous
           // 16-byte copies in flight; each thread copies, then reads, only its
           // own row.  Otherwise they are read from the workspace directly.
-          constexpr int kHalfRingF4 = (kRingBytes - kCsBytes) / 32;
+          constexpr int kHalfRingF4 = (G::kRingBytes - kCsBytes) / 32;
           const int per_chunk = n_oth * 8 * rv;           // float4 per column chunk
           const bool staged = final_item && per_chunk <= kHalfRingF4;
           int cpr = kChunks / 2;
@@ -995,6 +997,11 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   }
 }
 
+template <bool kPair>
+size_t tiled_smem_bytes() {
+  return 1024 /* alignment slack */ + Geo<kPair>::kRingBytes + sizeof(SmemBarriers);
+}
+
 template <typename E, int D, bool kBias, bool kPair>
 cudaError_t launch_one(int device, const CUtensorMap& tx, const CUtensorMap& tw,
                        const WriteParams& p, int grid, cudaStream_t stream) {
@@ -1002,7 +1009,7 @@ cudaError_t launch_one(int device, const CUtensorMap& tx, const CUtensorMap& tw,
   // the opt-in shared-memory size is set once per device and instantiation
   static std::atomic<uint64_t> attr_set{0};
   const uint64_t bit = 1ull << (device & 63);
-  const size_t smem = tiled_smem_bytes();
+  const size_t smem = tiled_smem_bytes<kPair>();
   if (!(attr_set.load() & bit)) {
     // setmaxnreg.inc waits until the CTA's register pool can grant it: the
     // pool the kernel launches with must cover the whole split, or it would
@@ -1064,9 +1071,6 @@ cudaError_t dispatch_plain(int device, int dtype, const CUtensorMap& tx, const C
 
 }  // namespace
 
-size_t tiled_smem_bytes() {
-  return 1024 /* alignment slack */ + kRingBytes + sizeof(SmemBarriers);
-}
 
 cudaError_t launch_tiled(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tx,
                          const CUtensorMap& tw, const WriteParams& p, int grid,
@@ -1095,12 +1099,12 @@ int pair_workers(int device) {
   if (n > 0) return n;
   auto kern = ctx_kv_tiled_kernel<__nv_bfloat16, 128, false, true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(tiled_smem_bytes())) != cudaSuccess)
+                           static_cast<int>(tiled_smem_bytes<true>())) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kTiledThreads, 1, 1);
-  cfg.dynamicSmemBytes = tiled_smem_bytes();
+  cfg.dynamicSmemBytes = tiled_smem_bytes<true>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;

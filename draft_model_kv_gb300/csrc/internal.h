@@ -65,7 +65,6 @@ constexpr int kMinUnitsPerCta = 8;   // k-blocks: keeps small problems from over
 constexpr int kMinSplitUnits = 2;    // k-blocks per worker of the leftover tiles (split-first order)
 constexpr int kStreamAutoMaxTokens = 64;    // AUTO picks the weight-streaming kernel up to here
 
-size_t tiled_smem_bytes();
 
 // Bytes of partial-tile workspace and arrival counters for a grid of `ctas`.
 inline size_t workspace_bytes(int ctas) {
