@@ -252,6 +252,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
           ok = 0;
         }
         if (!ok) pos = 0;
+        // the K tiles' epilogues read this token's cos/sin row
+        if (ok)
+          for (int b = 0; b < D * 4; b += 128) prefetch_l2(reinterpret_cast<const char*>(p.cos_sin + pos * D) + b);
       }
       sc->loc[t] = loc;
       sc->pos[t] = pos;
@@ -297,9 +300,18 @@ __global__ void __launch_bounds__(kSThreads, 1)
         c_first = sk_owner(p, u0);
         c_last = sk_owner(p, u0 + p.num_kb - 1);
       }
+      // A cut tile is finished by the contributor that holds its last k-block
+      // (c_last): that piece is the last item of c_last's backward walk.  The
+      // others publish their parts and never wait; c_last waits (bounded) for
+      // them, so it never spends a dump on its own part.  Waits only go from a
+      // worker to lower-numbered ones, and every CTA is resident (one per SM),
+      // so they end.  Before its accumulator is ready c_last looks whether the
+      // other parts are already published and, if there is exactly one,
+      // fetches its first 32 token columns.
+      const bool designated = cut && wid == c_last;
       bool early = false;
       float4 pre[8];
-      if (cut && final_item) {
+      if (designated) {
         if (r == 0) {
           const int seen = ld_acquire_gpu(p.counters + c_last);
           *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first;
@@ -307,8 +319,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         named_barrier(1, kSEpiThreads);
         early = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
         if (early && c_last - c_first == 1) {
-          const int other = c_first == wid ? c_last : c_first;
-          const float4* src = reinterpret_cast<const float4*>(ws_slot(p, other, other == c_first ? 1 : 0)) + r;
+          const float4* src = reinterpret_cast<const float4*>(ws_slot(p, c_first, 1)) + r;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             pre[j] = 4 * j < n_cols ? __ldcg(src + j * kSRows) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -334,26 +345,24 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tc_fence_after();
       const uint32_t t_acc = t_lane + acc * cfg.acc_stride;
 
-      // ---- a tile cut between CTAs (same protocol as the tiled kernel: the
-      // last contributor to arrive adds the parts in contributor order)
+      // ---- a tile cut between CTAs: publish this part, or (c_last) wait for
+      // the others and add the parts in contributor order
       bool finish = true;
       if (cut) {
         int32_t* counter = p.counters + c_last;
-        // every thread read the early flag before the barrier above
-        finish = early;
-        if (final_item && !finish) {
-          // the other parts may have been published while this CTA's MMAs
-          // ran: look again before spending a dump and a fixup read on it
-          if (r == 0) {
-            const int seen = ld_acquire_gpu(counter);
-            *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first;
+        finish = designated;
+        if (designated) {
+          bool ok = true;
+          if (!early && r == 0) ok = wait_count(counter, c_last - c_first, abort_flag, p.wait_limit_ns);
+          if (!named_barrier_and(1, kSEpiThreads, ok)) {
+            if (r == 0) {
+              *abort_flag = 1;
+              flag(p, DSPARK_FLAG_TIMEOUT);
+            }
+            break;
           }
-          named_barrier(1, kSEpiThreads);
-          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
-          named_barrier(1, kSEpiThreads);
-        }
-        if (finish && r == 0) *counter = 0;   // no other contributor touches it again
-        if (!finish) {
+          if (r == 0) *counter = 0;   // no other contributor touches it again
+        } else {
           float4* mine = reinterpret_cast<float4*>(ws_slot(p, wid, kb0 > 0 ? 0 : 1));
           for (int c = 0; c < n_cols; c += kSChunk) {
             uint32_t v[32];
@@ -366,15 +375,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             __syncwarp();
           }
           named_barrier(1, kSEpiThreads);   // every row of the part is written
-          if (threadIdx.x == 0) {
-            const int old = atom_add_acq_rel_gpu(counter, 1);
-            const int last = old == c_last - c_first;
-            if (last) *counter = 0;
-            *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
-          }
-          named_barrier(1, kSEpiThreads);
-          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
-          named_barrier(1, kSEpiThreads);
+          if (threadIdx.x == 0) atom_add_acq_rel_gpu(counter, 1);
         }
         if (tr != nullptr) {
           tr[1] |= (finish ? 2ull : 1ull) << 32;

@@ -115,17 +115,6 @@ __device__ __forceinline__ bool token_write(const WriteParams& p, int64_t t, boo
   return true;
 }
 
-// Bounded wait until *ctr >= target (acquire).
-__device__ __forceinline__ bool wait_count(const int32_t* ctr, int target, volatile int* abort_flag,
-                                           uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (ld_acquire_gpu(ctr) < target) {
-    if (*abort_flag != 0 || global_timer_ns() - t0 > limit_ns) return false;
-    __nanosleep(64);
-  }
-  return true;
-}
-
 __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }

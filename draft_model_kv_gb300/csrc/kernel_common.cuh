@@ -140,6 +140,18 @@ __device__ __forceinline__ int sk_owner(const WriteParams& p, int64_t u) {
   return static_cast<int>(((u + 1) * p.sk_workers - 1) / p.sk_units);
 }
 
+// Bounded wait until *ctr >= target (acquire): the arrival count of a split
+// tile's published parts.  False if this CTA aborted or the wait ran out.
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int target, volatile int* abort_flag,
+                                           uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_gpu(ctr) < target) {
+    if (*abort_flag != 0 || global_timer_ns() - t0 > limit_ns) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // Partial-tile slot of a CTA: [kTileN/4][kTileM] float4, so that the 32 rows
 // of a warp write one contiguous 512-byte run per 4 columns.
 constexpr int kSlotFloats = kTileM * kTileN;
