@@ -71,6 +71,7 @@ struct SmemBarriers {
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
+  uint64_t fix[2];      // per epilogue group: bulk copies of a split tile's other parts landed
   float ss_x[kTileM];   // plain mode: the second group's row sums of squares; split rows: per-warp sums
   uint32_t tmem_base;
   int abort;
@@ -329,6 +330,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       mbar_init(smem_u32(&bars->tmem_empty[b]), kPair ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->fix[0]), 1);
+    mbar_init(smem_u32(&bars->fix[1]), 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -520,6 +523,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const int ch_hi = ch_lo + kChunks / 2;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t fix_phase = 0;   // parity of this group's fix barrier
     int item = 0;
     WorkIter it = work_begin(p, wid, nw);
     int tile, kb0, kb1;
@@ -546,15 +550,26 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         const char* cs_row = reinterpret_cast<const char*>(p.cos_sin + pos * D);
         for (int b = group * 128; b < D * 4; b += 256) prefetch_l2(cs_row + b);
       }
-      // A CTA's last item is normally the last part of its split tile to be
-      // computed: check now, while its MMAs run, whether the other parts are
-      // already published (the decision is read after the barrier below).
+      // A tile cut between workers (whole-tiles-first order) is finished by
+      // the contributor that holds its last k-block: that piece is the last
+      // item of its backward walk.  The other contributors publish their parts
+      // and never wait; the finisher waits (bounded) for them, so it never
+      // spends a dump on its own part.  Waits only point to lower-numbered
+      // workers and every CTA is resident (at most one per SM), so they end.
+      // The finisher looks now, while its MMAs run, whether the other parts
+      // are already published (read after the barrier below).
       const bool cut = kb0 != 0 || kb1 != p.num_kb;
-      if (cut && final_item && etid == 0) {
+      int c_first = 0, c_last = 0;
+      if (cut) {
         const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
-        const int cf = sk_owner(p, u0), cl = sk_owner(p, u0 + p.num_kb - 1);
-        const int seen = ld_acquire_gpu(p.counters + (kPair ? 2 * cl + static_cast<int>(rank) : cl));
-        *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == cl - cf;
+        c_first = sk_owner(p, u0);
+        c_last = sk_owner(p, u0 + p.num_kb - 1);
+      }
+      auto cta_of = [&](int c) { return kPair ? 2 * c + static_cast<int>(rank) : c; };
+      const bool designated = cut && !p.sk_first && wid == c_last;
+      if (designated && etid == 0) {
+        const int seen = ld_acquire_gpu(p.counters + cta_of(c_last));
+        *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first;
       }
       // the outcome must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = mbar_wait_cluster(smem_u32(&bars->tmem_full[acc]), acc_phase, abort_flag,
@@ -604,38 +619,26 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           cp_async16(dst + static_cast<uint32_t>((u ^ (row & 7)) * 16), src + u * 16);
       };
 
-      // ---- a tile cut between CTAs: publish this part; the last contributor
-      // to arrive adds the other parts into its accumulator and finishes it
+      // ---- a tile cut between workers: publish this part, or (the
+      // finisher) wait for the other parts and add them in contributor order
       bool finish = true;
       if (cut) {
-        const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
-        // contributors are workers (CTAs, or CTA pairs whose halves are
-        // finished independently: the slot and counter of a pair CTA carry its rank)
-        const int c_first = sk_owner(p, u0);
-        const int c_last = sk_owner(p, u0 + p.num_kb - 1);
-        const int me = wid;
-        auto cta_of = [&](int c) { return kPair ? 2 * c + static_cast<int>(rank) : c; };
         int32_t* counter = p.counters + cta_of(c_last);
-        // If every other contributor had already published when the check
-        // above ran, this CTA finishes the tile without publishing its own
-        // part (the counter is reset: no other contributor touches it again).
-        // An earlier item of a CTA is almost never the last to arrive.
-        finish = final_item && *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
-        named_barrier(1, kEpiThreads);   // every thread has read the flag
-        if (final_item && !finish) {
-          // the other parts may have been published while this CTA's MMAs
-          // ran: look again before spending a dump and a fixup read on it
-          if (etid == 0) {
-            const int seen = ld_acquire_gpu(counter);
-            *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first;
+        finish = designated;
+        if (designated) {
+          const bool early = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
+          bool ok = true;
+          if (!early && etid == 0) ok = wait_count(counter, c_last - c_first, abort_flag, p.wait_limit_ns);
+          if (!named_barrier_and(1, kEpiThreads, ok)) {
+            if (etid == 0) {
+              *abort_flag = 1;
+              flag(p, DSPARK_FLAG_TIMEOUT);
+            }
+            break;
           }
-          named_barrier(1, kEpiThreads);
-          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
-          named_barrier(1, kEpiThreads);
-        }
-        if (finish && etid == 0) *counter = 0;
-        if (!finish) {
-          float4* mine = reinterpret_cast<float4*>(ws_slot(p, cta_of(me), kb0 > 0 ? 0 : 1));
+          if (etid == 0) *counter = 0;   // no other contributor touches it again
+        } else {
+          float4* mine = reinterpret_cast<float4*>(ws_slot(p, cta_of(wid), kb0 > 0 ? 0 : 1));
 #pragma unroll 1
           for (int ch = ch_lo; ch < ch_hi; ch += 2) {
             uint32_t v[32], u[32];
@@ -653,17 +656,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           }
           if (tr != nullptr) tr[3] = global_timer_ns();   // dump issued
           named_barrier(1, kEpiThreads);                  // every row of the part is written
-          if (etid == 0) {
-            const int old = atom_add_acq_rel_gpu(counter, 1);
-            // (split-first: every contributor finishes a share of the rows instead)
-            const int last = !p.sk_first && old == c_last - c_first;
-            if (last) *counter = 0;   // ready for the next launch
-            *reinterpret_cast<volatile int*>(&bars->last_arrival) = last;
-          }
+          if (etid == 0) atom_add_acq_rel_gpu(counter, 1);
           if (tr != nullptr) tr[4] = global_timer_ns();   // published
-          named_barrier(1, kEpiThreads);
-          finish = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
-          named_barrier(1, kEpiThreads);
         }
         if (tr != nullptr) {
           tr[1] |= (finish ? 2ull : 1ull) << 32;
@@ -672,45 +666,56 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         if (finish) {
           stage_cs();
           // accumulator = sum of all parts in ascending contributor order (this
-          // CTA's own part taken from TMEM at its place), so the result does not
-          // depend on which contributor arrived last.  Each group sums its half
-          // of the columns.
+          // CTA's own part taken from TMEM at its place), so the bits do not
+          // depend on timing.  Each group sums its half of the columns.
           const int64_t rows_left = static_cast<int64_t>(p.T) - row0;
           const int rv = rows_left <= 0 ? 0 : (rows_left < kTileM ? static_cast<int>(rows_left) : kTileM);
           const int n_oth = c_last - c_first;
-          // After the CTA's last MMA the operand ring is idle: the other parts
-          // are staged there (each group in its own half) with many asynchronous
-          // 16-byte copies in flight; each thread copies, then reads, only its
-          // own row.  Otherwise they are read from the workspace directly.
-          constexpr int kHalfRingF4 = (G::kRingBytes - kCsBytes) / 32;
-          const int per_chunk = n_oth * 8 * rv;           // float4 per column chunk
-          const bool staged = final_item && per_chunk <= kHalfRingF4;
-          int cpr = kChunks / 2;
-          if (staged && per_chunk > 0) {
-            cpr = kHalfRingF4 / per_chunk;                 // >= 1 here
+          // The operand ring is idle after the CTA's last MMA: the other parts
+          // are staged there (each group in its own half, after the cos/sin
+          // rows) with bulk copies, one per part and 32-column chunk (16 KB,
+          // contiguous in a workspace slot), completing on the group's
+          // mbarrier; each thread then reads its own row.  If the parts of
+          // one chunk do not fit, they are read from the workspace directly.
+          constexpr uint32_t kChunkBytes = 8 * kTileM * 16;
+          constexpr uint32_t kHalfRing = (G::kRingBytes - kCsBytes) / 2;
+          const bool staged = static_cast<uint32_t>(n_oth) * kChunkBytes <= kHalfRing;
+          int cpr = kChunks / 2;   // chunks per staging round
+          if (staged && n_oth > 0) {
+            cpr = static_cast<int>(kHalfRing / (static_cast<uint32_t>(n_oth) * kChunkBytes));
             cpr = cpr > kChunks / 2 ? kChunks / 2 : cpr;
           }
-          const uint32_t ring = smem_u32(smem) + kCsBytes + group * kHalfRingF4 * 16;
-          const float4* ring_f4 = reinterpret_cast<const float4*>(smem + kCsBytes) + group * kHalfRingF4;
+          const uint32_t ring = smem_u32(smem) + kCsBytes + static_cast<uint32_t>(group) * kHalfRing;
+          const float4* ring_f4 = reinterpret_cast<const float4*>(smem + kCsBytes + group * kHalfRing);
+          const uint32_t fbar = smem_u32(&bars->fix[group]);
+          const bool issuer = (etid % 128) == 0;
+          bool fix_ok = true;
 #pragma unroll 1
           for (int ch0 = ch_lo; ch0 < ch_hi; ch0 += cpr) {
             const int nch = (ch_hi - ch0) < cpr ? (ch_hi - ch0) : cpr;
-            if (staged && row < rv) {
-              int oi = 0;
-              for (int c = c_first; c <= c_last; ++c) {
-                if (c == me) continue;
-                const float4* src =
-                    reinterpret_cast<const float4*>(ws_slot(p, cta_of(c), c == c_first ? 1 : 0));
-                for (int cl = 0; cl < nch; ++cl)
-#pragma unroll
-                  for (int j = 0; j < 8; ++j)
-                    cp_async16(ring + 16u * static_cast<uint32_t>(((oi * nch + cl) * 8 + j) * rv + row),
-                               src + ((ch0 + cl) * 8 + j) * kTileM + row);
-                ++oi;
+            if (staged && n_oth > 0) {
+              if (issuer) {
+                // the group's reads of the previous round (generic proxy) come
+                // before this round's copies (async proxy) into the same bytes
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(fbar, static_cast<uint32_t>(n_oth * nch) * kChunkBytes);
+                int oi = 0;
+                for (int c = c_first; c <= c_last; ++c) {
+                  if (c == wid) continue;
+                  const float* slot = ws_slot(p, cta_of(c), c == c_first ? 1 : 0);
+                  for (int cl = 0; cl < nch; ++cl)
+                    bulk_load_g2s(ring + static_cast<uint32_t>(oi * nch + cl) * kChunkBytes,
+                                  slot + static_cast<size_t>(ch0 + cl) * 8 * kTileM * 4, kChunkBytes, fbar);
+                  ++oi;
+                }
               }
-              cp_async_wait_all();
+              // every thread of the group waits for the round's bytes (the
+              // copies read valid workspace and always complete: the wait
+              // does not stop on an abort, so none is left in flight)
+              int never = 0;
+              fix_ok = mbar_wait(fbar, fix_phase, &never, p.wait_limit_ns) && fix_ok;
+              fix_phase ^= 1u;
             }
-            const int stride = staged ? rv : kTileM;     // float4 between column groups
 #pragma unroll 1
             for (int cl = 0; cl < nch; ++cl) {
               const int ch = ch0 + cl;
@@ -718,17 +723,17 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
               int oi = 0;
               for (int c = c_first; c <= c_last; ++c) {
                 uint32_t part[32];
-                if (c == me) {
+                if (c == wid) {
                   tmem_ld32(t_row + ch * 32, part);   // warp-uniform branch
                 } else {
-                  if (row < rv) {
+                  if (row < rv && fix_ok) {
                     const float4* src =
-                        staged ? ring_f4 + (oi * nch + cl) * 8 * rv + row
+                        staged ? ring_f4 + (oi * nch + cl) * 8 * kTileM + row
                                : reinterpret_cast<const float4*>(ws_slot(p, cta_of(c), c == c_first ? 1 : 0)) +
                                      ch * 8 * kTileM + row;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                      const float4 q = src[j * stride];
+                      const float4 q = src[j * kTileM];
                       part[4 * j] = __float_as_uint(q.x);
                       part[4 * j + 1] = __float_as_uint(q.y);
                       part[4 * j + 2] = __float_as_uint(q.z);
@@ -747,6 +752,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
               __syncwarp();
               tmem_st32(t_row + ch * 32, v);
             }
+            // the group's staging half is rewritten by its next round
+            if (staged && n_oth > 0) named_barrier(2 + group, 128);
+          }
+          if (!fix_ok && etid % 128 == 0) {
+            *abort_flag = 1;
+            flag(p, DSPARK_FLAG_TIMEOUT);
           }
           // both groups' sums are in TMEM before any thread reads across halves
           tc_fence_before();

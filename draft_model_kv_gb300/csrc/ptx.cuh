@@ -366,6 +366,15 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// Bulk copy global -> shared memory of this CTA without a tensor map,
+// completion counted (bytes) on the mbarrier `bar`: both addresses 16-byte
+// aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+               "l"(gsrc), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Arrival on a GPU-scope counter with acquire-release semantics.  Called by
 // one thread after a CTA barrier, the release covers every write that the
 // CTA's threads made before the barrier (release is cumulative), and the
