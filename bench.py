@@ -361,7 +361,7 @@ NCU_TRAFFIC = {
     # (workload, tokens) -> per-launch DRAM bytes (read + write) of the fused
     # kernel from one ncu capture of the kernel as it stands (summaries under
     # profiles/); anything without a capture of the current kernel reports null
-    ("decode512", 512): 90.609664e6 + 12.175360e6,
+    ("decode512", 512): 90.666496e6 + 12.352512e6,
     ("decode512", 16): 84.096512e6 + 2.558720e6,
 }
 
@@ -807,7 +807,7 @@ def run_combine(args):
 COMBINE_NCU_TRAFFIC = {
     # (workload, tokens) -> per-launch DRAM bytes of the main_proj product
     # kernel from an ncu capture of the kernel as it stands; null without one
-    ("prefill32k", 4096): 488.811008e6 + 43.305728e6,
+    ("prefill32k", 4096): 486.317312e6 + 43.308544e6,
 }
 
 
