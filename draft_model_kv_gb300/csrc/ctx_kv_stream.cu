@@ -51,7 +51,7 @@ struct StreamBarriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int last_arrival;
+  int last_arrival;   // finisher's early look: every other part of its cut tile already published
 };
 
 // Epilogue scratch after the barriers.

@@ -75,7 +75,7 @@ struct SmemBarriers {
   float ss_x[kTileM];   // plain mode: the second group's row sums of squares; split rows: per-warp sums
   uint32_t tmem_base;
   int abort;
-  int last_arrival;   // set by the epilogue leader when this CTA finishes a cut tile
+  int last_arrival;   // finisher's early look: every other part of its cut tile already published
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk,

@@ -33,7 +33,8 @@ struct WriteParams {
   // waves; the other tiles' k-blocks (sk_units of them) are cut into
   // sk_workers equal contiguous ranges ("stream-K").  Two orders:
   //  - sk_first = 0: the whole tiles first, then the cut ranges; a cut tile is
-  //    finished by whichever contributor arrives last (no CTA waits for another)
+  //    finished by the contributor holding its last k-block, which waits
+  //    (bounded) for the others' parts; the others never wait
   //  - sk_first = 1: the cut ranges first, every part published; once all parts
   //    of a cut tile are published, each contributor sums and finishes its own
   //    share of the tile's rows, while its whole tiles run on the tensor cores

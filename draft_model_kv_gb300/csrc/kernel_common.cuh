@@ -86,9 +86,9 @@ __device__ __forceinline__ void st16(void* dst, uint32_t a, uint32_t b, uint32_t
 // schedule is split-first.  In the other order the backward walk makes a
 // worker begin with the (usually small) first k-blocks of the tile at the end
 // of its range, publish that part while it computes the rest, and end with
-// the (usually large) last part of the tile at the start of its range, which
-// it then finishes itself: the partial tile it holds in TMEM is the last to
-// arrive.
+// the (usually large) last part of the tile at the start of its range: it
+// holds that tile's last k-block and finishes the tile from the partial tile
+// it holds in TMEM plus the parts the others published.
 struct WorkIter {
   int dp_tile, nw;
   int64_t start, cur;
