@@ -21,7 +21,7 @@ __all__ = [
     "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
-    "dspark_set_kernel_variant", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
+    "dspark_set_kernel_variant", "dspark_describe_schedule", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
     "dspark_correct_drafts_and_bonus", "dspark_draft_attention", "dspark_draft_attention_workspace_bytes",
     "Combine", "dspark_pack_combine", "dspark_combine_hidden_states", "dspark_combine_get_status",
     "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
@@ -440,6 +440,17 @@ def dspark_combine_get_status(c: Combine, stream=None) -> int:
     _abi.check(load().dspark_combine_get_status(c.handle, _stream_handle(stream), ctypes.byref(flags)),
                "dspark_combine_get_status")
     return flags.value
+
+
+def dspark_describe_schedule(tiles: int, num_kb: int, workers: int, split_first_allowed: bool = True) -> dict:
+    """The work split of the tiled kernels for `tiles` output tiles of
+    `num_kb` k-blocks on up to `workers` workers (host only): workers,
+    whole_tiles, split_units, split_workers, split_first."""
+    import ctypes
+    info = _abi.ScheduleInfo()
+    _abi.check(load().dspark_describe_schedule(int(tiles), int(num_kb), int(workers), int(bool(split_first_allowed)),
+                                               ctypes.byref(info)), "dspark_describe_schedule")
+    return {name: getattr(info, name) for name, _ in info._fields_}
 
 
 def dspark_set_kernel_variant(bundle: Bundle, variant: str) -> None:

@@ -35,7 +35,7 @@ EXPORTS = (
     "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv", "dspark_write_ctx_kv",
     "dspark_get_device_status", "dspark_clear_device_status", "dspark_bundle_get_info",
     "dspark_free_bundle", "dspark_status_string", "dspark_set_trace_buffer",
-    "dspark_write_ctx_kv_noalloc", "dspark_set_kernel_variant",
+    "dspark_write_ctx_kv_noalloc", "dspark_set_kernel_variant", "dspark_describe_schedule",
 )
 
 
@@ -52,6 +52,13 @@ class LayerDesc(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
         ("eps", ctypes.c_float),
+    ]
+
+
+class ScheduleInfo(ctypes.Structure):
+    _fields_ = [
+        ("workers", ctypes.c_int32), ("whole_tiles", ctypes.c_int32), ("split_units", ctypes.c_int64),
+        ("split_workers", ctypes.c_int32), ("split_first", ctypes.c_int32),
     ]
 
 
@@ -103,6 +110,8 @@ def load() -> ctypes.CDLL:
     lib.dspark_write_ctx_kv_noalloc.restype = ctypes.c_int
     lib.dspark_set_kernel_variant.argtypes = [vp, i32]
     lib.dspark_set_kernel_variant.restype = ctypes.c_int
+    lib.dspark_describe_schedule.argtypes = [i64, i32, i32, i32, ctypes.POINTER(ScheduleInfo)]
+    lib.dspark_describe_schedule.restype = ctypes.c_int
     lib.dspark_set_trace_buffer.argtypes = [vp, vp, i64]
     lib.dspark_set_trace_buffer.restype = ctypes.c_int
     lib.dspark_qk_norm_rope.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, i64, i32, i32, i32,

@@ -378,6 +378,20 @@ int dspark_set_trace_buffer(dspark_bundle_t b, uint64_t* buf, int64_t words) {
   return DSPARK_OK;
 }
 
+int dspark_describe_schedule(int64_t tiles, int32_t num_kb, int32_t workers, int32_t split_first_allowed,
+                             dspark_schedule_info* out) {
+  if (out == nullptr || tiles < 1 || tiles > 0x7FFFFFFF || num_kb < 1 || workers < 1) return DSPARK_E_INVALID_ARG;
+  WriteParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int grid = plan_schedule(static_cast<int>(tiles), num_kb, workers, split_first_allowed != 0, p);
+  out->workers = grid;
+  out->whole_tiles = p.dp_tiles;
+  out->split_units = p.sk_units;
+  out->split_workers = p.sk_workers;
+  out->split_first = p.sk_first;
+  return DSPARK_OK;
+}
+
 int dspark_bundle_get_info(dspark_bundle_t b, dspark_bundle_info* info) {
   if (b == nullptr || info == nullptr) return DSPARK_E_INVALID_ARG;
   info->num_layers = b->L;

@@ -260,6 +260,29 @@ DSPARK_API int dspark_set_trace_buffer(dspark_bundle_t bundle, uint64_t* buf, in
 
 DSPARK_API int dspark_bundle_get_info(dspark_bundle_t bundle, dspark_bundle_info* info /* (host) */);
 
+/* Work split of the tiled kernels (host only; needs no GPU). (host) */
+typedef struct dspark_schedule_info {
+  int32_t workers;        /* workers launched (CTAs, or CTA pairs) */
+  int32_t whole_tiles;    /* tiles 0 .. whole_tiles-1 are computed whole, tile w, w+workers, ... by worker w */
+  int64_t split_units;    /* k-blocks of the remaining tiles, cut into contiguous ranges */
+  int32_t split_workers;  /* workers 0 .. split_workers-1 take one range each (equal shares) */
+  int32_t split_first;    /* 1: ranges before whole tiles, every contributor finishes rows of its
+                             cut tiles; 0: whole tiles first, a cut tile finished by the owner of
+                             its last k-block */
+} dspark_schedule_info;
+
+/*
+ * dspark_describe_schedule -- the work split a write (or the combine product)
+ * uses for a problem of `tiles` output tiles with `num_kb` 64-deep k-blocks
+ * each on up to `workers` workers (SMs for single-CTA tiles, SM pairs for CTA
+ * pairs).  `split_first_allowed` is 1 for the tiled kernels and 0 for the
+ * weight-streaming kernel.  Diagnostics: the kernels compute the same split
+ * themselves.  Returns DSPARK_E_INVALID_ARG for non-positive sizes or a NULL
+ * `out`.
+ */
+DSPARK_API int dspark_describe_schedule(int64_t tiles, int32_t num_kb, int32_t workers,
+                                        int32_t split_first_allowed, dspark_schedule_info* out /* (host) */);
+
 /* Release the bundle's device memory (synchronises the device first). NULL is a no-op. */
 DSPARK_API void dspark_free_bundle(dspark_bundle_t bundle);
 
