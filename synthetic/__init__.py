@@ -29,7 +29,7 @@ the request count).
 from __future__ import annotations
 
 import dataclasses
-from typing import Dict, List, Optional
+from typing import Dict, List, Optional, Sequence
 
 import numpy as np
 
@@ -332,12 +332,15 @@ class AttnWorkload:
 
 def make_attention_workload(batch: int, block: int, num_q_heads: int, num_kv_heads: int, D: int,
                             ctx_lo: int, ctx_hi: int, slack: int = 64, dtype: str = BF16,
-                            seed: int = 6) -> AttnWorkload:
-    """Per request a context length U[ctx_lo, ctx_hi] of distinct random pool
-    slots (pool = total context + slack slots); q, keys and values N(0,1) in
-    the model dtype; sm_scale = D**-0.5."""
+                            seed: int = 6, contexts: Optional[Sequence[int]] = None) -> AttnWorkload:
+    """Per request a context length U[ctx_lo, ctx_hi] (or the given
+    `contexts`) of distinct random pool slots (pool = total context + slack
+    slots); q, keys and values N(0,1) in the model dtype; sm_scale = D**-0.5."""
     rng = np.random.default_rng(seed)
     ctx = rng.integers(ctx_lo, ctx_hi + 1, size=batch)
+    if contexts is not None:
+        ctx = np.asarray(contexts, dtype=np.int64)
+        assert ctx.shape == (batch,)
     slots = int(ctx.sum()) + slack
     idx = rng.permutation(slots)[:int(ctx.sum())].astype(np.int64)
     start = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int64)

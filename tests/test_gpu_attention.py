@@ -69,6 +69,18 @@ def test_matches_oracle(batch, block, nq, nkv, D, lo, hi, dtype):
     check(a, out)
 
 
+def test_bench_launch_configuration_sampled():
+    """The bench's launch configuration (64 requests of 8 x 32 heads over 8 KV
+    heads of 128, bf16, contexts up to 32768: the same context split and
+    waves) with one 32768-token context and 63 short ones; the long request
+    and two short ones are checked against the oracle."""
+    ctx = [32768] + [int(c) for c in np.random.default_rng(11).integers(1, 200, size=63)]
+    a = synthetic.make_attention_workload(64, 8, 32, 8, 128, 0, 0, contexts=ctx)
+    out, flags = run(a, max_context=32768)
+    assert flags == 0
+    check(a, out, requests=[0, 1, 63])
+
+
 def test_bad_index_is_flagged_and_skipped():
     a = synthetic.make_attention_workload(3, 8, 32, 8, 128, 20, 60)
     idx = a.kv_indices.copy()
