@@ -59,6 +59,15 @@ def test_decode512_shapes_sampled():
     check(cw, out, rows=np.concatenate([[0], rows, [cw.T - 1]]))
 
 
+def test_4096_tokens_sampled():
+    # the bench's second configuration: 16 x 16 pair tiles (three waves and a
+    # leftover, whole tiles first); rows of the first, middle and last blocks
+    cw = synthetic.make_combine_workload("prefill32k", tokens=4096)
+    out = run(cw)
+    rows = np.sort(np.random.default_rng(5).choice(cw.T, size=40, replace=False))
+    check(cw, out, rows=np.concatenate([[0, 255, 256, 2047], rows, [cw.T - 1]]))
+
+
 @pytest.mark.parametrize("name,T", [("fp16bias", 64), ("k3gqa", 40)])
 def test_other_shapes(name, T):
     cw = synthetic.make_combine_workload(name, tokens=T)

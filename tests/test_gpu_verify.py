@@ -20,7 +20,7 @@ def _require_gpu():
     build.build()
 
 
-@pytest.mark.parametrize("batch,block", [(64, 8), (1000, 16), (7, 1), (33, 33), (300, 70), (1, 2)])
+@pytest.mark.parametrize("batch,block", [(64, 8), (4096, 8), (1000, 16), (7, 1), (33, 33), (300, 70), (1, 2)])
 def test_matches_oracle(batch, block):
     import draft_model_kv_gb300 as dk
     cand, tgt = synthetic.make_verify_workload(batch, block, seed=batch + block)
