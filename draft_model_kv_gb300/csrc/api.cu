@@ -334,6 +334,7 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
   p.num_tiles = p.num_m * p.num_n;
   const int workers = plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : b->sms, true, p);
+  give_leftover_to_v_tiles(p, workers);
   const int grid = pair ? 2 * workers : workers;
   const cudaError_t e =
       pair ? launch_pair(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w_half, p, grid, stream)

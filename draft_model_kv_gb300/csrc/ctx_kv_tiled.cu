@@ -78,17 +78,6 @@ struct SmemBarriers {
   int last_arrival;   // finisher's early look: every other part of its cut tile already published
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk,
-                                            int& n_blk) {
-  const int group_size = kGroupM * num_n;
-  const int group = tile / group_size;
-  const int first_m = group * kGroupM;
-  const int gm = min(num_m - first_m, kGroupM);
-  const int r = tile - group * group_size;
-  m_blk = first_m + r % gm;
-  n_blk = r / gm;
-}
-
 // Whether token t's rows are written, with its pool slot and position (sglang
 // PR #31847 summary page, fused_kv_norm_rope_write: loc < 0 skips the token;
 // in window mode column t mod W must be below commit_lens[t div W]).  Range

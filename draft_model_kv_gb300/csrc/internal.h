@@ -8,6 +8,8 @@
 
 namespace dspark {
 
+constexpr int kMaxDpPerm = 160;   // whole tiles that a launch may reorder (one wave of SMs)
+
 // Everything the fused write needs besides the two operand tensor maps.
 struct WriteParams {
   int32_t T, H, N, L, NH, D, KV;
@@ -42,15 +44,21 @@ struct WriteParams {
   int64_t sk_units;
   int32_t sk_workers;
   int32_t sk_first;
+  // optional order of the whole tiles: worker w's i-th whole tile is
+  // dp_perm[w + i*workers] when that index is below dp_perm_n (else itself)
+  int32_t dp_perm_n;
   uint64_t* trace;              // null, or [gridDim.x][kTraceWords] timeline stamps
   float* workspace;             // [gridDim.x][2][kTileN/4][kTileM][4] fp32 partial tiles
   int32_t* counters;            // [gridDim.x] arrivals per cut tile, reset by the last one
   uint64_t wait_limit_ns;       // bound on any single in-kernel wait
+  int16_t dp_perm[kMaxDpPerm];
   void* k_pool[DSPARK_MAX_LAYERS];
   void* v_pool[DSPARK_MAX_LAYERS];
   int64_t k_stride[DSPARK_MAX_LAYERS];
   int64_t v_stride[DSPARK_MAX_LAYERS];
 };
+
+static_assert(sizeof(WriteParams) <= 4000, "kernel parameter space");
 
 // Tiled tcgen05 path: one CTA per SM, 128-token x 256-column output tiles.
 constexpr int kTileM = 128;
@@ -60,10 +68,23 @@ constexpr int kTiledThreads = 384;   // 3 warpgroups: 2 epilogue, 1 control
 constexpr int kLaunchRegs = 168;     // registers per thread at launch (65536 / 384, rounded down to 8)
 constexpr int kGroupM = 8;     // m-blocks per raster group (L2 reuse of weight tiles)
 
+// Output tile `tile` -> (token block, column block): tiles are rastered in
+// groups of kGroupM token blocks so that weight tiles are reused from L2.
+__host__ __device__ inline void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_blk) {
+  const int group_size = kGroupM * num_n;
+  const int group = tile / group_size;
+  const int first_m = group * kGroupM;
+  const int gm = num_m - first_m < kGroupM ? num_m - first_m : kGroupM;
+  const int r = tile - group * group_size;
+  m_blk = first_m + r % gm;
+  n_blk = r / gm;
+}
+
 constexpr int kTraceWords = 64;      // per CTA: start, end, items, 6 words per work item; last: split rows done
 constexpr int kTraceItems = (kTraceWords - 3) / 6;
 constexpr int kMinUnitsPerCta = 8;   // k-blocks: keeps small problems from over-splitting
 constexpr int kMinSplitUnits = 2;    // k-blocks per worker of the leftover tiles (split-first order)
+constexpr int kMaxLightShare = 8;    // k-blocks per V-tile worker when only those take the leftover
 constexpr int kStreamAutoMaxTokens = 64;    // AUTO picks the weight-streaming kernel up to here
 
 
@@ -111,6 +132,39 @@ inline int plan_schedule(int tiles, int num_kb, int workers, bool split_first, W
   }
   p.sk_workers = grid;
   return grid;
+}
+
+// Split-first order with exactly one whole tile per worker: hand the leftover
+// k-blocks only to the workers whose whole tile holds no K head (a V tile's
+// epilogue has no norm and no rotation: it is the shorter one), so that both
+// kinds of worker end together.  Reorders the whole tiles so that those
+// workers come first (p.dp_perm) and narrows p.sk_workers to them; applied
+// when each of them then takes kMinSplitUnits to kMaxLightShare k-blocks.
+// The fused write only (head_dim 64 or 128).
+inline void give_leftover_to_v_tiles(WriteParams& p, int workers) {
+  if (!p.sk_first || p.D == 0 || p.dp_tiles != workers || workers > kMaxDpPerm) return;
+  int16_t light[kMaxDpPerm], heavy[kMaxDpPerm];
+  int nl = 0, nh = 0;
+  for (int t = 0; t < p.dp_tiles; ++t) {
+    int m_blk, n_blk;
+    tile_coords(t, p.num_m, p.num_n, m_blk, n_blk);
+    bool has_k = false;
+    for (int seg = 0; seg < kTileN / p.D; ++seg) {
+      const int c0 = n_blk * kTileN + seg * p.D;
+      if (c0 < p.N && c0 % (2 * p.KV) < p.KV) has_k = true;
+    }
+    if (has_k)
+      heavy[nh++] = static_cast<int16_t>(t);
+    else
+      light[nl++] = static_cast<int16_t>(t);
+  }
+  if (nl == 0 || nl >= p.sk_workers || p.sk_units < static_cast<int64_t>(nl) * kMinSplitUnits ||
+      p.sk_units > static_cast<int64_t>(nl) * kMaxLightShare)
+    return;
+  p.sk_workers = nl;
+  for (int w = 0; w < nl; ++w) p.dp_perm[w] = light[w];
+  for (int w = 0; w < nh; ++w) p.dp_perm[nl + w] = heavy[w];
+  p.dp_perm_n = p.dp_tiles;
 }
 
 // Launch the fused kernel for the bundle dtype (1 = bf16, 2 = fp16).  Returns

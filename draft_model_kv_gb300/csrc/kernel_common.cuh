@@ -106,10 +106,14 @@ __device__ __forceinline__ WorkIter work_begin(const WriteParams& p, int wid, in
   return it;
 }
 
+__device__ __forceinline__ int dp_tile_at(const WriteParams& p, int i) {
+  return i < p.dp_perm_n ? static_cast<int>(p.dp_perm[i]) : i;
+}
+
 __device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, int& tile, int& kb0,
                                           int& kb1) {
   if (!p.sk_first && it.dp_tile < p.dp_tiles) {
-    tile = it.dp_tile;
+    tile = dp_tile_at(p, it.dp_tile);
     kb0 = 0;
     kb1 = p.num_kb;
     it.dp_tile += it.nw;
@@ -126,7 +130,7 @@ __device__ __forceinline__ bool work_next(const WriteParams& p, WorkIter& it, in
     return true;
   }
   if (p.sk_first && it.dp_tile < p.dp_tiles) {
-    tile = it.dp_tile;
+    tile = dp_tile_at(p, it.dp_tile);
     kb0 = 0;
     kb1 = p.num_kb;
     it.dp_tile += it.nw;
