@@ -277,8 +277,11 @@ typedef struct dspark_schedule_info {
  * each on up to `workers` workers (SMs for single-CTA tiles, SM pairs for CTA
  * pairs).  `split_first_allowed` is 1 for the tiled kernels and 0 for the
  * weight-streaming kernel.  Diagnostics: the kernels compute the same split
- * themselves.  Returns DSPARK_E_INVALID_ARG for non-positive sizes or a NULL
- * `out`.
+ * themselves.  One refinement is not shown: in the split-first order with
+ * one whole tile per worker, the write hands the leftover only to the
+ * workers whose whole tile holds V heads (when each then takes 2 to 8
+ * k-blocks), reordering the whole tiles so that those workers come first.
+ * Returns DSPARK_E_INVALID_ARG for non-positive sizes or a NULL `out`.
  */
 DSPARK_API int dspark_describe_schedule(int64_t tiles, int32_t num_kb, int32_t workers,
                                         int32_t split_first_allowed, dspark_schedule_info* out /* (host) */);
