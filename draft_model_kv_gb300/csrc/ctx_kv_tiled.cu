@@ -1,10 +1,18 @@
 // Fused stacked-KV projection + K RMSNorm + table neox RoPE + pool scatter on
 // tcgen05 tensor cores (sm_103a).
 //
-// One persistent CTA per SM walks 128-token x 256-column tiles of the stacked
-// output Y = ctx_hidden . W_all^T (W_all rows: l0:K, l0:V, l1:K, ...; sglang
-// PR #31986 summary page, _stacked_ctx_kv_params).  256 columns are whole
-// heads (D = 64 or 128), so each tile's epilogue can finish its heads alone.
+// One persistent CTA per SM (or CTA pair per SM pair) walks 128-token (256
+// for a pair) x 256-column tiles of the stacked output Y = ctx_hidden .
+// W_all^T (W_all rows: l0:K, l0:V, l1:K, ...; sglang PR #31986 summary page,
+// _stacked_ctx_kv_params).  256 columns are whole heads (D = 64 or 128), so
+// each tile's epilogue can finish its heads alone.  The work split
+// (plan_schedule, internal.h) mixes whole tiles with tiles whose k-blocks are
+// cut between workers; a cut tile is finished from the published fp32 parts
+// either by the owner of its last k-block (whole tiles first) or row-wise by
+// every contributor (split-first, for one wave plus a small leftover).
+//
+// With tcgen05.mma.cta_group::2 the leader CTA of a pair issues 256x256x16
+// MMAs over both CTAs' operand halves; commits are multicast to both.
 //
 //   warps 0..7  epilogue, two warpgroups that take alternate heads of a tile:
 //               each thread owns one token row of the accumulator
@@ -13,8 +21,9 @@
 //               thread's registers; then 16-byte stores into the pool row
 //   warp 8      TMA producer: X and W_all K-slices into a smem ring (4 stages,
 //               or 5 for CTA pairs)
-//   warp 9      MMA issuer: tcgen05.mma 128x256x16 into one of two TMEM
-//               accumulators (2 x 256 fp32 columns); owns TMEM alloc/free
+//   warp 9      MMA issuer: tcgen05.mma 128x256x16 (256x256x16 for a pair)
+//               into one of two TMEM accumulators (2 x 256 fp32 columns);
+//               owns TMEM alloc/free
 //   warps 10,11 idle (they complete the control warpgroup)
 // Registers are moved to the epilogue with setmaxnreg (control warpgroup 40,
 // epilogue warpgroups 232 per thread).
