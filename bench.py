@@ -15,7 +15,9 @@ before its start event fires (a short device-side delay precedes it).  `e2e` is 
 through the public API with pinned host inputs: host->device copies of the
 step's inputs, the write, and a device->host read of the status word, timed
 on the host.  `--impl reference` times the CPU oracle instead (the reference
-arm of this build: there is no other implementation to run).
+arm of this build: there is no other implementation to run).  `--trace`
+prints per-CTA timelines of traced writes instead (diagnostics, not a bench
+line).
 """
 from __future__ import annotations
 
@@ -831,6 +833,70 @@ def make(args):
     return synthetic.make_workload(args.workload, **kw)
 
 
+def run_trace(args, w):
+    """One JSON line per traced launch of the write (`--trace`): per-CTA
+    timeline percentiles (min / median / max, microseconds from the first CTA
+    start) read from the library's trace buffer (dspark_set_trace_buffer).
+    Diagnostics only: not a bench line."""
+    import numpy as np
+    import torch
+    import draft_model_kv_gb300 as dk
+    from draft_model_kv_gb300 import build as _build
+    from synthetic.device import stage
+
+    _build.build()
+    st = stage(w, device="cuda")
+    bundle = dk.dspark_pack_ctx_kv(st["layers"], w.H)
+    pools = dk.dspark_bind_pools(bundle, st["k_pools"], st["v_pools"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    words = 64
+    buf = torch.zeros(sms * words, dtype=torch.int64, device="cuda")
+
+    def step():
+        dk.dspark_write_ctx_kv(bundle, st["ctx_hidden"], st["positions"], st["cos_sin"], st["cache_loc"], pools,
+                               commit_lens=st["commit_lens"], loc_row_width=st["loc_row_width"])
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    dk.dspark_set_trace_buffer(bundle, buf)
+    lines = []
+    for k in range(args.steps):
+        buf.zero_()
+        flush.fill_(2)
+        torch.cuda.synchronize()
+        step()
+        torch.cuda.synchronize()
+        tr = buf.view(sms, words).cpu().numpy().astype(np.int64)
+        tr = tr[tr[:, 0] > 0]
+        t0 = tr[:, 0].min()
+        us = lambda v: (v - t0) / 1e3
+
+        def pct(v):
+            v = np.asarray(v, dtype=np.float64)
+            return [round(float(x), 2) for x in np.percentile(v, [0, 50, 100])] if v.size else None
+
+        # the kernels stamp their first (words - 3) // 6 items: the last-item
+        # fields cover the CTAs whose every item was stamped
+        full = tr[(tr[:, 2] >= 1) & (tr[:, 2] <= (words - 3) // 6)]
+        last = full[:, 2] - 1
+        rows = np.arange(full.shape[0])
+        lines.append({
+            "trace": k, "workload": w.name, "tokens": w.T, "ctas": int(tr.shape[0]),
+            "items": pct(tr[:, 2]),
+            "start_us": pct(us(tr[:, 0])),
+            "first_item_ready_us": pct(us(tr[tr[:, 2] >= 1, 5])),
+            "split_rows_done_us": pct(us(tr[tr[:, words - 1] > 0, words - 1])),
+            "last_item_ready_us": pct(us(full[rows, 3 + 6 * last + 2])),
+            "last_item_done_us": pct(us(full[rows, 3 + 6 * last + 5])),
+            "end_us": pct(us(tr[:, 1])),
+        })
+    dk.dspark_set_trace_buffer(bundle, None)
+    bundle.free()
+    return lines
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -843,6 +909,8 @@ def main(argv=None):
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", action="store_true",
+                    help="print per-CTA timelines of --steps traced writes instead of a bench line")
     ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify", "attention", "combine"],
                     help="qk_norm_rope: the draft layers' in-place QK-norm + RoPE; verify: the "
                          "verify step's accepted-draft count and bonus token (instead of the write)")
@@ -863,6 +931,12 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
+    if args.trace:
+        if args.op != "ctx_kv" or ws > 1:
+            ap.error("--trace times the write on one GPU")
+        for line in run_trace(args, make(args)):
+            print(json.dumps(line))
+        return 0
     if args.op == "qk_norm_rope":
         out = run_qk(args)
     elif args.op == "verify":
