@@ -15,7 +15,7 @@ before its start event fires (a short device-side delay precedes it).  `e2e` is 
 through the public API with pinned host inputs: host->device copies of the
 step's inputs, the write, and a device->host read of the status word, timed
 on the host.  `--impl reference` times the CPU oracle instead (the reference
-arm of this build: there is no other implementation to run).  `--trace`
+arm: there is no other implementation to run).  `--trace`
 prints per-CTA timelines of traced writes instead (diagnostics, not a bench
 line).
 """
