@@ -12,6 +12,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
                          quarter-turn table, hand-worked golden example
   written_tokens         hand-worked window golden example, -1 / commit edge cases
   write_target_hidden_kv composition of the above + bias closed form
+  eager=True (diagnostic) closed forms for both rounding points (projection,
+                         normed K); agrees with the pure reading within the
+                         parity tolerance
 
 and of the in-place QK RMSNorm + table RoPE (``qk_norm_rope.py``, pinned in
 ``tests/test_oracle_qknorm_pins.py``):

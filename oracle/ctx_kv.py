@@ -30,6 +30,10 @@ notes):
   * k_norm weights are converted to fp32 (PR #31986 page: stacked ``.float()``).
   * No intermediate rounding: values stay in the accumulation precision until
     the store (the fused kernel's body is not shown on the PR #31847 page).
+    ``eager=True`` is the other reading, kept as a diagnostic: the eager path
+    rounds the projection (the linear layer's output) and the normalised K
+    (the PR #31847 QK kernel rounds before the rotation "to match eager") to
+    the model dtype.
   * In window mode a token is also skipped when its loc is -1; commit_lens[b]
     above W acts as W, and 0 writes nothing.
   * pos outside [0, max_pos), loc >= pool_slots and duplicate written locs are
@@ -189,10 +193,19 @@ def apply_k_rope(positions: np.ndarray, k: np.ndarray, cos_sin: np.ndarray,
     return np.concatenate([o1, o2], axis=-1).reshape(k.shape)
 
 
+def _round(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round to the nearest value of the model dtype (ties to even), in the
+    accumulation precision."""
+    from .qk_norm_rope import round_to
+    return round_to(x, dtype).astype(x.dtype)
+
+
 def per_layer_reference(ctx_hidden: np.ndarray, layers: Sequence[LayerDesc],
-                        positions: np.ndarray, cos_sin: np.ndarray, acc=np.float64
-                        ) -> Tuple[List[np.ndarray], List[np.ndarray]]:
-    """K (normed, roped) and V of every layer as [T, num_kv_heads, head_dim]."""
+                        positions: np.ndarray, cos_sin: np.ndarray, acc=np.float64,
+                        eager: bool = False) -> Tuple[List[np.ndarray], List[np.ndarray]]:
+    """K (normed, roped) and V of every layer as [T, num_kv_heads, head_dim].
+    With ``eager`` the projection and the normalised K are rounded to the
+    model dtype (the eager path's intermediate roundings)."""
     ks, vs = [], []
     for lay in layers:
         dt = lay.weight_dtype
@@ -203,8 +216,12 @@ def per_layer_reference(ctx_hidden: np.ndarray, layers: Sequence[LayerDesc],
         w = widen(lay.qkv_weight[rows], dt, acc)
         b = None if lay.qkv_bias is None else widen(lay.qkv_bias[rows], dt, acc)
         k, v = kv_proj_only(x, w, b, 0, kv_size)
+        if eager:
+            k, v = _round(k, dt), _round(v, dt)
         kn = widen(lay.k_norm_weight, lay.k_norm_dtype or dt, np.float32).astype(acc)
         k = apply_k_norm(k, kn, lay.eps, lay.num_kv_heads, lay.head_dim)
+        if eager:
+            k = _round(k, dt)
         k = apply_k_rope(positions, k, cos_sin, lay.num_kv_heads, lay.head_dim)
         ks.append(k.reshape(-1, lay.num_kv_heads, lay.head_dim))
         vs.append(v.reshape(-1, lay.num_kv_heads, lay.head_dim))
@@ -286,7 +303,7 @@ def write_target_hidden_kv(ctx_hidden: np.ndarray, layers: Sequence[LayerDesc],
                            commit_lens: Optional[np.ndarray] = None,
                            loc_row_width: Optional[int] = None,
                            sample: Optional[np.ndarray] = None,
-                           acc=np.float64) -> WriteResult:
+                           acc=np.float64, eager: bool = False) -> WriteResult:
     """The whole write: what every pool row holds afterwards.
 
     The pool slot set is decided from cache_loc / commit_lens over all tokens;
@@ -305,7 +322,7 @@ def write_target_hidden_kv(ctx_hidden: np.ndarray, layers: Sequence[LayerDesc],
     pos = positions[toks]
     if pos.size and (pos.min() < 0 or pos.max() >= cos_sin.shape[0]):
         raise WriteArgError("position outside the cos/sin table")
-    ks, vs = per_layer_reference(ctx_hidden[toks], layers, pos, cos_sin, acc)
+    ks, vs = per_layer_reference(ctx_hidden[toks], layers, pos, cos_sin, acc, eager)
     return WriteResult(tokens=toks, slots=cache_loc[toks], k=np.stack(ks), v=np.stack(vs))
 
 
@@ -318,9 +335,9 @@ def layer_descs(workload) -> List[LayerDesc]:
             for l in workload.layers]
 
 
-def run_workload(workload, sample=None, acc=np.float64) -> WriteResult:
+def run_workload(workload, sample=None, acc=np.float64, eager: bool = False) -> WriteResult:
     w = workload
     return write_target_hidden_kv(
         w.ctx_hidden, layer_descs(w), w.positions, w.cos_sin, w.cache_loc, w.pool_slots,
         w.commit_lens, w.loc_row_width if w.commit_lens is not None else None,
-        sample=sample, acc=acc)
+        sample=sample, acc=acc, eager=eager)

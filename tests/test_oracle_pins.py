@@ -7,6 +7,7 @@ hand-worked examples stored under tests/golden/.  Together they are chosen so
 that a dropped term, a wrong sign or index, a transposed operand, a K/V swap,
 a layer mix-up or an off-by-one in the window rule fails at least one of them.
 """
+import functools
 import json
 import math
 import os
@@ -367,3 +368,53 @@ def test_fp32_oracle_within_small_fraction_of_tolerance():
     err = np.abs(r64.k - r32.k.astype(np.float64)).max()
     err_v = np.abs(r64.v - r32.v.astype(np.float64)).max()
     assert err < 2e-2 / 100 and err_v < 2e-2 / 100
+
+
+# ---------------------------------------------------------------------------
+# the eager-rounding reading (diagnostic mode of the oracle)
+# ---------------------------------------------------------------------------
+
+def test_eager_rounding_rounds_the_projection_and_the_normed_k():
+    """Closed forms for where the eager reading rounds.  V: hidden [1, 1] and
+    a V row [1, 2**-10] give 1 + 2**-10, which bf16 (8 significant bits)
+    rounds to 1.0 -- the pure reading keeps 1 + 2**-10.  K: a constant head of
+    3 with eps 0 normalises to w exactly (no rounding to see), while a head
+    [3, 4, 0, ...] normalises to (3, 4) / rms and the eager reading rounds those
+    values to bf16 before the (identity) rotation."""
+    D, H = 64, 2
+    wv = np.zeros((D, H), np.float32)
+    wv[0] = [1.0, 2.0 ** -10]
+    wk = np.zeros((D, H), np.float32)
+    wk[:, 0] = 3.0
+    lay = make_layer(wk, wv, np.ones(D), eps=0.0, q_rows=2)
+    x = bf(np.array([[1.0, 1.0]], np.float32))
+    pos = np.zeros(1, np.int64)
+    tab = identity_table(1, D)
+    ks, vs = oracle.per_layer_reference(x, [lay], pos, tab)
+    ke, ve = oracle.per_layer_reference(x, [lay], pos, tab, eager=True)
+    assert vs[0][0, 0, 0] == 1.0 + 2.0 ** -10 and ve[0][0, 0, 0] == 1.0
+    np.testing.assert_array_equal(ks[0], ke[0])           # 3 / 3 * 1: representable
+    wk2 = np.zeros((D, H), np.float32)
+    wk2[0, 0], wk2[1, 0] = 3.0, 4.0
+    lay2 = make_layer(wk2, wv, np.ones(D), eps=0.0, q_rows=2)
+    ks2, _ = oracle.per_layer_reference(x, [lay2], pos, tab)
+    ke2, _ = oracle.per_layer_reference(x, [lay2], pos, tab, eager=True)
+    r = math.sqrt(25.0 / D)
+    np.testing.assert_allclose(ks2[0][0, 0, :2], [3 / r, 4 / r], rtol=1e-15)
+    np.testing.assert_array_equal(ke2[0][0, 0, :2], oracle.round_to(np.array([3 / r, 4 / r]), "bf16"))
+
+
+@functools.lru_cache(maxsize=1)
+def _decode_shapes_8():
+    return synthetic.make_workload("decode512", tokens=8)
+
+
+def test_eager_and_pure_readings_agree_within_the_tolerance():
+    """The two readings of the unshown fused kernel's rounding differ by far
+    less than the parity tolerance, so either is a valid reference."""
+    w = _decode_shapes_8()
+    a = oracle.run_workload(w)
+    b = oracle.run_workload(w, eager=True)
+    for x, y in ((a.k, b.k), (a.v, b.v)):
+        assert np.all(np.abs(x - y) <= 2e-2 + 2e-2 * np.abs(x))
+    assert not np.array_equal(a.k, b.k)
