@@ -2,9 +2,11 @@
 
 One step = one dspark_write_ctx_kv call over the whole workload: the stacked
 K|V projection of every token, K RMSNorm, table RoPE and the scatter into
-every layer's pool.  Default workload: the Qwen3-8B-shaped draft decode
-(T=512 = 64 requests x 8-token windows, H=4096, 5 layers, 8 kv heads x 128,
-bf16, commit_lens truncation, 65536-slot pools).
+every layer's pool.  Default workload: the prefill-sized context write
+(T=32768 = 8 requests x 4096 tokens, H=4096, 5 layers, 8 kv heads x 128,
+bf16, 1% of the slots -1, 40000-slot pools), the largest configuration and
+the one the tensor-core target is stated on; `--workload decode512` (64
+requests x 8-token windows) and `--tokens T` give the other lines.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -327,12 +329,13 @@ def run_gpu(args, w):
     achieved_tf = flops / (mean_ms * 1e-3) / 1e12
     achieved_gb = bytes_ / (mean_ms * 1e-3) / 1e9
     bound = "tensor" if t_tc >= t_hbm else "hbm"
-    traffic = ncu_traffic(w.name, w.T)
+    traffic, traffic_note = ncu_traffic("ctx_kv", w.name, w.T)
     roof_tc = {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16_tflops"],
                "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16_tflops"], "traffic": traffic,
+               "traffic_source": traffic_note,
                "peak_source": pk["source"] + " (burst: the kernel is timed alone)"}
     roof_hbm = {"bound": "hbm", "achieved": achieved_gb, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved_gb / pk["hbm_gbs"], "traffic": traffic,
+                "frac": achieved_gb / pk["hbm_gbs"], "traffic": traffic, "traffic_source": traffic_note,
                 "peak_source": pk["source"]}
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -359,17 +362,56 @@ def run_gpu(args, w):
     return out
 
 
-NCU_TRAFFIC = {
-    # (workload, tokens) -> per-launch DRAM bytes (read + write) of the fused
-    # kernel from one ncu capture of the kernel as it stands (summaries under
-    # profiles/); anything without a capture of the current kernel reports null
-    ("decode512", 512): 88.996608e6 + 6.560000e6,
-    ("decode512", 16): 84.096512e6 + 2.558720e6,
+# Per-launch DRAM bytes (read + write) of each op's dominant kernel come from
+# one ncu capture each, recorded in profiles/dram_traffic.md with the hash of
+# the kernel's sources at capture time.  A line whose kernel sources have
+# changed since, or that has no capture, reports traffic null with the reason.
+KERNEL_SOURCES = {
+    "ctx_kv": ["ctx_kv_tiled.cu", "ctx_kv_stream.cu", "kernel_common.cuh", "internal.h", "ptx.cuh",
+               "api.cu"],
+    "qk_norm_rope": ["qk_norm_rope.cu"],
+    "attention": ["draft_attention.cu"],
+    "combine": ["ctx_kv_tiled.cu", "kernel_common.cuh", "internal.h", "ptx.cuh", "combine.cu"],
 }
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
 
-def ncu_traffic(name, tokens):
-    return NCU_TRAFFIC.get((name, tokens))
+def source_hash(op):
+    """First 12 hex digits of the sha256 of the op's kernel sources."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[op]:
+        with open(os.path.join(ROOT, "draft_model_kv_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read().replace(b"\r\n", b"\n") + b"\0")
+    return h.hexdigest()[:12]
+
+
+def traffic_rows(path=TRAFFIC_TABLE):
+    """Rows of the traffic table: dicts with op, workload, tokens, kernel,
+    hash, read, write, summary."""
+    rows = []
+    if not os.path.exists(path):
+        return rows
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) != 8 or not cells[2].isdigit():
+            continue
+        rows.append({"op": cells[0], "workload": cells[1], "tokens": int(cells[2]), "kernel": cells[3],
+                     "hash": cells[4].strip("`"), "read": int(cells[5]), "write": int(cells[6]),
+                     "summary": cells[7].strip("`")})
+    return rows
+
+
+def ncu_traffic(op, workload, tokens):
+    """(bytes per launch or None, note) for the bench line's roofline."""
+    now = source_hash(op)
+    found = [r for r in traffic_rows() if (r["op"], r["workload"], r["tokens"]) == (op, workload, tokens)]
+    if not found:
+        return None, f"no ncu capture of this op at {workload} / {tokens} tokens in profiles/dram_traffic.md"
+    r = found[-1]
+    if r["hash"] != now:
+        return None, f"kernel sources changed since the ncu capture (captured {r['hash']}, now {now})"
+    return float(r["read"] + r["write"]), f"ncu capture, profiles/{r['summary']}"
 
 
 QK_METRIC = "QK-norm+RoPE tokens/s (in place over the Q and K heads of the fused QKV rows)"
@@ -431,6 +473,7 @@ def run_qk(args):
     bytes_ = q.T * nqk * 2 * 2 + q.T * 8 + q.T * q.D * 4
     pk = peaks()
     achieved = bytes_ * args.steps / dev_s / 1e9
+    traffic, traffic_note = ncu_traffic("qk_norm_rope", q.name, q.T)
     # end to end: pinned host rows and positions in, the pass, the status word out
     host_x = x.cpu().pin_memory()
     host_pos = pos.cpu().pin_memory()
@@ -460,8 +503,8 @@ def run_qk(args):
                    "parallelism": "replicas (one independent pass per GPU, no collective)",
                    "l2": "flushed between steps (256 MiB write)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": QK_NCU_TRAFFIC.get((q.name, q.T)),
-                     "peak_source": pk["source"]},
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "traffic_source": traffic_note, "peak_source": pk["source"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": host_x.numel() * 2 + q.T * 8,
                 "d2h_bytes_per_step": 4, "steps": e2e_steps,
                 "timing": "host wall clock per step: h2d rows + positions, the pass, status d2h + sync"},
@@ -643,6 +686,8 @@ def run_attention(args):
     bytes_ = ctx_total * (nkv * D * 2 * 2 + 8) + rows * (nq + 2 * nkv) * D * 2 + rows * nq * D * 2
     pk = peaks()
     achieved = bytes_ * args.steps / dev_s / 1e9
+    attn_name = "decode_mix" if args.tokens is None else f"ctx{args.tokens}"
+    traffic, traffic_note = ncu_traffic("attention", attn_name, rows)
     # end to end: the block's q / k / v from pinned host memory, the attention, the output back
     hq, hk, hv = q.cpu().pin_memory(), ke.cpu().pin_memory(), ve.cpu().pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -671,8 +716,8 @@ def run_attention(args):
                    "max_context": max_ctx, "parallelism": "replicas (one independent pass per GPU, no collective)",
                    "l2": "flushed between steps (256 MiB write); inputs larger than L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": ATTN_NCU_TRAFFIC.get((batch, ctx_total)),
-                     "peak_source": pk["source"]},
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "traffic_source": traffic_note, "peak_source": pk["source"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": rows * (nq + 2 * nkv) * D * 2,
                 "d2h_bytes_per_step": rows * nq * D * 2, "steps": e2e_steps},
         "gpu_launches": 2 * args.steps,
@@ -771,12 +816,14 @@ def run_combine(args):
     e2e_value, _, _ = aggregate(cw.T * e2e_steps, e2e_total)
     if rank != 0:
         return None
+    traffic, traffic_note = ncu_traffic("combine", args.workload, cw.T)
     tensor = {"bound": "tensor", "achieved": flops / t_step / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
               "frac": flops / t_step / 1e12 / pk["bf16_tflops"],
-              "traffic": COMBINE_NCU_TRAFFIC.get((args.workload, cw.T)),
+              "traffic": traffic, "traffic_source": traffic_note,
               "peak_source": pk["source"] + " (burst: the kernel is timed alone)"}
     hbm = {"bound": "hbm", "achieved": bytes_ / t_step / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
-           "frac": bytes_ / t_step / 1e9 / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"]}
+           "frac": bytes_ / t_step / 1e9 / pk["hbm_gbs"], "traffic": traffic, "traffic_source": traffic_note,
+           "peak_source": pk["source"]}
     t_tc, t_hbm = flops / (pk["bf16_tflops"] * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9)
     primary, other = (tensor, hbm) if t_tc >= t_hbm else (hbm, tensor)
     res = {
@@ -804,27 +851,6 @@ def run_combine(args):
                                "sample": f"{rows} tokens x {reps} runs, {el:.1f} s, numpy float64"}
     c.free()
     return res
-
-
-COMBINE_NCU_TRAFFIC = {
-    # (workload, tokens) -> per-launch DRAM bytes of the main_proj product
-    # kernel from an ncu capture of the kernel as it stands; null without one
-    ("prefill32k", 4096): 486.317312e6 + 43.308544e6,
-}
-
-
-ATTN_NCU_TRAFFIC = {
-    # (requests, total context tokens) -> per-launch DRAM bytes of the split
-    # kernel from an ncu capture of the kernel as it stands; null without one
-    (64, 262144): 1082.343e6 + 44.051456e6,
-}
-
-
-QK_NCU_TRAFFIC = {
-    # (workload, tokens) -> per-launch DRAM bytes of dspark_qk_norm_rope's kernel
-    # from an ncu capture of the kernel as it stands; null without one
-    ("prefill32k", 32768): 341.093888e6 + 274.807552e6,
-}
 
 
 def make(args):
@@ -902,7 +928,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="decode512")
+    ap.add_argument("--workload", default="prefill32k")
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count override (supplementary sweeps; keeps the workload's other sizes)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -914,7 +940,12 @@ def main(argv=None):
     ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify", "attention", "combine"],
                     help="qk_norm_rope: the draft layers' in-place QK-norm + RoPE; verify: the "
                          "verify step's accepted-draft count and bonus token (instead of the write)")
+    ap.add_argument("--source-hash", default=None, choices=sorted(KERNEL_SOURCES),
+                    help="print the hash of an op's kernel sources (the key of profiles/dram_traffic.md) and exit")
     args = ap.parse_args(argv)
+    if args.source_hash is not None:
+        print(source_hash(args.source_hash))
+        return 0
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     import synthetic

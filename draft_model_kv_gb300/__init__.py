@@ -20,7 +20,7 @@ from ._abi import (DSparkError, FLAG_LOC_RANGE, FLAG_POS_RANGE, FLAG_TIMEOUT,  #
 __all__ = [
     "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
     "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
-    "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc",
+    "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc", "dspark_set_split_wait_test",
     "dspark_set_kernel_variant", "dspark_describe_schedule", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
     "dspark_correct_drafts_and_bonus", "dspark_draft_attention", "dspark_draft_attention_workspace_bytes",
     "Combine", "dspark_pack_combine", "dspark_combine_hidden_states", "dspark_combine_get_status",
@@ -163,6 +163,18 @@ def dspark_bind_pools(bundle: Bundle, k_pools, v_pools) -> PoolSet:
     return ps
 
 
+def _check_token_shapes(ctx_hidden, positions, cache_loc, cos_sin, hidden: int, head_dim: int) -> None:
+    """The sizes the C ABI takes on trust: one position and one loc per token,
+    hidden columns, and cos/sin rows of head_dim values."""
+    T = ctx_hidden.shape[0]
+    if ctx_hidden.shape[1] != hidden:
+        raise ValueError(f"ctx_hidden has {ctx_hidden.shape[1]} columns, the layers take {hidden}")
+    if positions.numel() != T or cache_loc.numel() != T:
+        raise ValueError("positions and cache_loc must hold one entry per token")
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != head_dim or cos_sin.shape[0] < 1:
+        raise ValueError(f"cos_sin must be [max_pos, head_dim={head_dim}]")
+
+
 def dspark_write_ctx_kv(bundle: Bundle, ctx_hidden, positions, cos_sin, cache_loc, k_pools,
                         v_pools=None, commit_lens=None, loc_row_width: Optional[int] = None,
                         stream=None) -> None:
@@ -185,6 +197,7 @@ def dspark_write_ctx_kv(bundle: Bundle, ctx_hidden, positions, cos_sin, cache_lo
             raise TypeError(f"{name} must be a contiguous {dt} tensor")
     if commit_lens is not None and (commit_lens.dtype != torch.int32 or not commit_lens.is_contiguous()):
         raise TypeError("commit_lens must be a contiguous int32 tensor")
+    _check_token_shapes(ctx_hidden, positions, cache_loc, cos_sin, bundle.hidden, bundle.head_dim)
     if isinstance(k_pools, PoolSet):
         if v_pools is not None or k_pools.num_layers != bundle.num_layers:
             raise ValueError("a PoolSet of this bundle's layer count goes alone in k_pools")
@@ -224,6 +237,15 @@ def dspark_set_trace_buffer(bundle: Bundle, buf) -> None:
     _abi.check(code, "dspark_set_trace_buffer")
 
 
+def dspark_set_split_wait_test(bundle: Bundle, missing_arrivals: int, limit_ns: int = 0) -> None:
+    """Diagnostics for tests of the timeout path: later writes with `bundle`
+    wait for `missing_arrivals` more published parts of every cut tile than
+    exist, each such wait bounded by `limit_ns`, so those waits run out and the
+    write reports DSPARK_FLAG_TIMEOUT.  0 restores normal writes."""
+    _abi.check(load().dspark_set_split_wait_test(bundle.handle, int(missing_arrivals), int(limit_ns)),
+               "dspark_set_split_wait_test")
+
+
 def dspark_write_ctx_kv_noalloc(stacked_weight, k_norm_weight, eps: float, num_layers: int,
                                 num_kv_heads: int, head_dim: int, ctx_hidden, positions, cos_sin,
                                 cache_loc, k_pools, v_pools, stacked_bias=None, commit_lens=None,
@@ -239,6 +261,11 @@ def dspark_write_ctx_kv_noalloc(stacked_weight, k_norm_weight, eps: float, num_l
     device array inside the library (at most 64 SMs per call).  Calls share
     that array, so calls whose kernels overlap on the GPU race: keep them
     ordered.  Make the first call on a device before any stream capture.
+    status_flags: a one-element int32 CUDA tensor that receives the device
+    flags (out-of-range position or slot, a wait that ran out); with None
+    those flags are discarded and cannot be read back.  Sizes are checked
+    here, before the library is called, since the C entry point has no
+    bundle to check them against.
     """
     import torch
     T = ctx_hidden.shape[0]
@@ -256,11 +283,30 @@ def dspark_write_ctx_kv_noalloc(stacked_weight, k_norm_weight, eps: float, num_l
         raise TypeError("commit_lens must be a contiguous int32 tensor")
     if len(k_pools) != num_layers or len(v_pools) != num_layers:
         raise ValueError("one K and one V pool per layer")
+    # the C ABI takes these sizes on trust (there is no bundle to check them
+    # against): a mismatch would make the kernel read past a tensor
+    n_rows = num_layers * 2 * num_kv_heads * head_dim
+    hidden = stacked_weight.shape[1]
+    if stacked_weight.shape[0] != n_rows:
+        raise ValueError(f"stacked_weight must have num_layers*2*num_kv_heads*head_dim = {n_rows} rows, "
+                         f"got {stacked_weight.shape[0]}")
+    if tuple(k_norm_weight.shape) != (num_layers, head_dim):
+        raise ValueError(f"k_norm_weight must be [num_layers, head_dim] = [{num_layers}, {head_dim}]")
+    if stacked_bias is not None and (stacked_bias.numel() != n_rows or not stacked_bias.is_contiguous()):
+        raise ValueError(f"stacked_bias must be a contiguous [{n_rows}] tensor")
+    _check_token_shapes(ctx_hidden, positions, cache_loc, cos_sin, hidden, head_dim)
+    slots = k_pools[0].shape[0]
+    for p in list(k_pools) + list(v_pools):
+        if (p.dim() != 3 or p.shape[0] != slots or p.shape[1] != num_kv_heads or p.shape[2] != head_dim
+                or p.stride(1) != head_dim or p.stride(2) != 1):
+            raise ValueError("pools must be [slots, num_kv_heads, head_dim] with strides (*, head_dim, 1) "
+                             "and one slot count")
+    if status_flags is not None and (status_flags.numel() < 1 or status_flags.element_size() != 4):
+        raise TypeError("status_flags must be a 4-byte integer CUDA tensor")
     dt = stacked_weight.dtype
     for t in [ctx_hidden] + list(k_pools) + list(v_pools) + ([] if stacked_bias is None else [stacked_bias]):
         if t.dtype != dt:
             raise TypeError("weights, hidden, bias and pools must share one dtype")
-    slots = k_pools[0].shape[0]
     width = 0 if loc_row_width is None else int(loc_row_width)
     nwin = 0 if commit_lens is None else commit_lens.numel()
     kstr = (ctypes.c_int64 * num_layers)(*[p.stride(0) for p in k_pools])

@@ -36,6 +36,7 @@ EXPORTS = (
     "dspark_get_device_status", "dspark_clear_device_status", "dspark_bundle_get_info",
     "dspark_free_bundle", "dspark_status_string", "dspark_set_trace_buffer",
     "dspark_write_ctx_kv_noalloc", "dspark_set_kernel_variant", "dspark_describe_schedule",
+    "dspark_set_split_wait_test",
 )
 
 
@@ -114,6 +115,8 @@ def load() -> ctypes.CDLL:
     lib.dspark_describe_schedule.restype = ctypes.c_int
     lib.dspark_set_trace_buffer.argtypes = [vp, vp, i64]
     lib.dspark_set_trace_buffer.restype = ctypes.c_int
+    lib.dspark_set_split_wait_test.argtypes = [vp, i32, ctypes.c_uint64]
+    lib.dspark_set_split_wait_test.restype = ctypes.c_int
     lib.dspark_qk_norm_rope.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, i64, i32, i32, i32,
                                         ctypes.c_float, vp, vp]
     lib.dspark_qk_norm_rope.restype = ctypes.c_int

@@ -92,6 +92,8 @@ struct dspark_bundle {
   int sms;              // SM count of the bundle's device
   uint64_t* trace;      // optional timeline buffer (dspark_set_trace_buffer)
   int variant;          // DSPARK_VARIANT_* (dspark_set_kernel_variant)
+  int split_wait_extra;        // dspark_set_split_wait_test: arrivals no worker will make
+  uint64_t split_wait_ns;      // bound on the waits for a cut tile's published parts
   CUtensorMap tmap_w_half;   // W_all with 128-row boxes (CTA-pair kernel)
   float eps;
   CUtensorMap tmap_w;
@@ -187,6 +189,8 @@ int dspark_pack_ctx_kv(const dspark_layer_desc* layers, int32_t num_layers, int3
   b->N = static_cast<int64_t>(num_layers) * 2 * b->KV;
   b->w_pitch = (hidden + 7) / 8 * 8;   // 16-byte row pitch for TMA
   b->eps = f.eps;
+  b->split_wait_extra = 0;
+  b->split_wait_ns = kWaitLimitNs;
   b->sms = device_sm_count(device);
   if (b->sms <= 0) {
     delete b;
@@ -292,7 +296,9 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   p.workspace = b->workspace;
   p.counters = b->counters;
   p.trace = b->trace;
-  p.wait_limit_ns = 2000000000ull;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.split_wait_ns = b->split_wait_ns;
+  p.split_wait_extra = b->split_wait_extra;
   for (int l = 0; l < b->L; ++l) {
     p.k_pool[l] = k_pools[l];
     p.v_pool[l] = v_pools[l];
@@ -316,7 +322,9 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
     p.num_m = 1;
     p.num_n = static_cast<int32_t>(b->N / 128);
     p.num_tiles = p.num_n;
-    const int grid = plan_schedule(p.num_tiles, p.num_kb, b->sms, false, p);
+    const int resident = stream_workers(device, stages, stage_b);
+    if (resident <= 0) return DSPARK_E_CUDA;
+    const int grid = plan_schedule(p.num_tiles, p.num_kb, resident < b->sms ? resident : b->sms, false, p);
     const cudaError_t e = launch_stream(device, b->dtype, b->D, b->bias != nullptr, tmap_x, b->tmap_w_half, p,
                                         t_pad, stages, stage_b, acc_stride, tmem_cols, grid, stream);
     return e == cudaSuccess ? DSPARK_OK : DSPARK_E_CUDA;
@@ -329,11 +337,17 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   // are asked for or the device has fewer than two SMs
   const int pairs = b->variant != DSPARK_VARIANT_SINGLE ? pair_workers(device) : 0;
   const bool pair = pairs > 0;
+  int singles = 0;
+  if (!pair) {
+    singles = single_workers(device);
+    if (singles <= 0) return DSPARK_E_CUDA;
+    if (singles > b->sms) singles = b->sms;
+  }
   const int tile_rows = pair ? 2 * kTileM : kTileM;
   p.num_m = static_cast<int32_t>((T + tile_rows - 1) / tile_rows);
   p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
   p.num_tiles = p.num_m * p.num_n;
-  const int workers = plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : b->sms, true, p);
+  const int workers = plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : singles, true, p);
   give_leftover_to_v_tiles(p, workers);
   const int grid = pair ? 2 * workers : workers;
   const cudaError_t e =
@@ -348,6 +362,19 @@ int dspark_set_kernel_variant(dspark_bundle_t b, int32_t variant) {
       variant != DSPARK_VARIANT_STREAM)
     return DSPARK_E_INVALID_ARG;
   b->variant = variant;
+  return DSPARK_OK;
+}
+
+int dspark_set_split_wait_test(dspark_bundle_t b, int32_t missing_arrivals, uint64_t limit_ns) {
+  if (b == nullptr || missing_arrivals < 0 || missing_arrivals > 1024) return DSPARK_E_INVALID_ARG;
+  if (missing_arrivals == 0) {
+    b->split_wait_extra = 0;
+    b->split_wait_ns = kWaitLimitNs;
+    return DSPARK_OK;
+  }
+  if (limit_ns == 0 || limit_ns > kWaitLimitNs) return DSPARK_E_INVALID_ARG;
+  b->split_wait_extra = missing_arrivals;
+  b->split_wait_ns = limit_ns;
   return DSPARK_OK;
 }
 

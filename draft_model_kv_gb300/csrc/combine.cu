@@ -198,7 +198,9 @@ int dspark_combine_hidden_states(dspark_combine_t c, const void* aux, int64_t T,
   p.status = c->status;
   p.workspace = c->workspace;
   p.counters = c->counters;
-  p.wait_limit_ns = 2000000000ull;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.split_wait_ns = kWaitLimitNs;
+  p.split_wait_extra = 0;
   p.y = ctx_hidden;
   p.y_stride = out_row_stride;
   p.rowsq = c->rowsq;

@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (designated) {
         if (r == 0) {
           const int seen = ld_acquire_gpu(p.counters + c_last);
-          *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first;
+          *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first + p.split_wait_extra;
         }
         named_barrier(1, kSEpiThreads);
         early = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
@@ -353,7 +353,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         finish = designated;
         if (designated) {
           bool ok = true;
-          if (!early && r == 0) ok = wait_count(counter, c_last - c_first, abort_flag, p.wait_limit_ns);
+          if (!early && r == 0)
+            ok = wait_count(counter, c_last - c_first + p.split_wait_extra, abort_flag, p.split_wait_ns);
           if (!named_barrier_and(1, kSEpiThreads, ok)) {
             if (r == 0) {
               *abort_flag = 1;
@@ -536,6 +537,30 @@ cudaError_t launch_stream_one(int device, const CUtensorMap& tx, const CUtensorM
 }  // namespace
 
 size_t stream_max_smem_bytes() { return 227 * 1024; }
+
+int stream_workers(int device, int stages, uint32_t stage_b) {
+  // CTAs of the streaming kernel that can be resident at once with this
+  // launch's shared memory (every instantiation has the same block size and
+  // shared memory): the split-tile waits assume all of the grid is resident
+  // (cached per device and token padding: stage_b = t_pad * 128 bytes)
+  static std::atomic<int> cache[64][kSMaxTokens / 16 + 1];
+  const int d = device & 63, k = static_cast<int>(stage_b / (16 * kTileK * 2)) % (kSMaxTokens / 16 + 1);
+  int n = cache[d][k].load();
+  if (n > 0) return n;
+  auto kern = ctx_kv_stream_kernel<__nv_bfloat16, 128, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(stream_max_smem_bytes())) != cudaSuccess)
+    return 0;
+  int per_sm = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, stream_smem_bytes(stages, stage_b)) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || per_sm <= 0 ||
+      sms <= 0)
+    return 0;
+  // one CTA per SM at most: a second one would halve each CTA's ring
+  cache[d][k].store(sms);
+  return sms;
+}
 
 bool stream_plan(int64_t T, int* t_pad, int* stages, uint32_t* stage_b, uint32_t* acc_stride,
                  uint32_t* tmem_cols) {

@@ -118,6 +118,26 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 
+// Give up after a wait ran out: report the timeout and stop this CTA's work.
+// A pair stops both CTAs (the flag is also set in the peer's shared memory):
+// their loads complete on the leader's barriers and are released by the
+// leader's MMAs, so one CTA alone cannot wind the pipeline down.  The peer is
+// still resident here: both CTAs meet at a cluster barrier before exiting.
+template <bool kPair>
+__device__ __forceinline__ void abort_work(const WriteParams& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  if constexpr (kPair)
+    st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), cluster_ctarank() ^ 1u), 1u);
+  flag(p, DSPARK_FLAG_TIMEOUT);
+}
+
+// After an abort a pair's producers may have stopped at different stages: a
+// leader barrier armed for bytes the peer never loaded, or a peer load the
+// leader's MMA never released, is never observed complete.  Their drain then
+// ends on this bound rather than the full wait bound: every load in question
+// was issued before the abort, and a tile load lands within microseconds.
+constexpr uint64_t kPairAbortDrainNs = 200000;
+
 // The cut tiles of the split-first schedule (the tiles left over after the
 // full wave, whose k-blocks are spread over the workers).  Every contributor
 // publishes its part before any is read; then contributor i of n finishes
@@ -160,7 +180,7 @@ __device__ bool finish_split_rows(const WriteParams& p, int wid, int nw, uint32_
     int32_t* counter = p.counters + cta_of(cl);
     bool ok = true;
     if (etid == 0) {
-      ok = wait_count(counter, n, abort_flag, p.wait_limit_ns);
+      ok = wait_count(counter, n + p.split_wait_extra, abort_flag, p.split_wait_ns);
       // second round: the last contributor past the wait resets the counter
       // for the next launch (every contributor has already read it as n)
       if (ok && atom_add_acq_rel_gpu(counter, 1) == 2 * n - 1) *counter = 0;
@@ -408,23 +428,24 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             }
           }
         }
-        if (!ok) {
-          *abort_flag = 1;
-          flag(p, DSPARK_FLAG_TIMEOUT);
-        }
+        if (!ok) abort_work<kPair>(p, abort_flag);
         // every load issued must land before the CTA may exit (bounded by time
         // only: an abort must not cut this wait short).  A pair's peer sees its
         // loads land only through the leader's MMA releasing the stage.
         int never = 0;
+        const bool short_drain = kPair && *abort_flag != 0;
+        const uint64_t t_end = global_timer_ns() + (short_drain ? kPairAbortDrainNs : p.wait_limit_ns);
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
           if (uses[s] == 0) continue;
+          const uint64_t now = global_timer_ns();
+          const uint64_t lim = short_drain ? (now < t_end ? t_end - now : 0) : p.wait_limit_ns;
           if (!kPair)
-            mbar_wait(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
+            mbar_wait(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, lim);
           else if (leader)
-            mbar_wait_cluster(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
+            mbar_wait_cluster(smem_u32(&bars->full[s]), (uses[s] - 1u) & 1u, &never, lim);
           else
-            mbar_wait_cluster(smem_u32(&bars->empty[s]), (uses[s] - 1u) & 1u, &never, p.wait_limit_ns);
+            mbar_wait_cluster(smem_u32(&bars->empty[s]), (uses[s] - 1u) & 1u, &never, lim);
         }
       }
     } else if (warp == kMmaWarp) {
@@ -485,10 +506,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             acc_phase ^= 1u;
           }
         }
-        if (!ok) {
-          *abort_flag = 1;
-          flag(p, DSPARK_FLAG_TIMEOUT);
-        }
+        if (!ok) abort_work<kPair>(p, abort_flag);
         if (issued) {
           // all MMAs issued by this thread complete before TMEM is released
           if (kPair)
@@ -567,7 +585,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const bool designated = cut && !p.sk_first && wid == c_last;
       if (designated && etid == 0) {
         const int seen = ld_acquire_gpu(p.counters + cta_of(c_last));
-        *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first;
+        *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first + p.split_wait_extra;
       }
       // the outcome must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = mbar_wait_cluster(smem_u32(&bars->tmem_full[acc]), acc_phase, abort_flag,
@@ -585,10 +603,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // every epilogue warp takes the same decision (they meet at named
       // barriers below), and every wait ends within its time bound
       if (!named_barrier_and(1, kEpiThreads, got)) {
-        if (etid == 0) {
-          *abort_flag = 1;
-          flag(p, DSPARK_FLAG_TIMEOUT);
-        }
+        if (etid == 0) abort_work<kPair>(p, abort_flag);
         break;
       }
       tc_fence_after();
@@ -626,12 +641,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         if (designated) {
           const bool early = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
           bool ok = true;
-          if (!early && etid == 0) ok = wait_count(counter, c_last - c_first, abort_flag, p.wait_limit_ns);
+          if (!early && etid == 0)
+            ok = wait_count(counter, c_last - c_first + p.split_wait_extra, abort_flag, p.split_wait_ns);
           if (!named_barrier_and(1, kEpiThreads, ok)) {
-            if (etid == 0) {
-              *abort_flag = 1;
-              flag(p, DSPARK_FLAG_TIMEOUT);
-            }
+            if (etid == 0) abort_work<kPair>(p, abort_flag);
             break;
           }
           if (etid == 0) *counter = 0;   // no other contributor touches it again
@@ -753,10 +766,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             // the group's staging half is rewritten by its next round
             if (staged && n_oth > 0) named_barrier(2 + group, 128);
           }
-          if (!fix_ok && etid % 128 == 0) {
-            *abort_flag = 1;
-            flag(p, DSPARK_FLAG_TIMEOUT);
-          }
+          if (!fix_ok && etid % 128 == 0) abort_work<kPair>(p, abort_flag);
           // both groups' sums are in TMEM before any thread reads across halves
           tc_fence_before();
           named_barrier(1, kEpiThreads);
@@ -961,10 +971,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       }
       if (reduce_after) {
         if (!finish_split_rows<E, D, kBias, kPair>(p, wid, nw, rank, bars->ss_x, abort_flag)) {
-          if (etid == 0) {
-            *abort_flag = 1;
-            flag(p, DSPARK_FLAG_TIMEOUT);
-          }
+          if (etid == 0) abort_work<kPair>(p, abort_flag);
           break;
         }
         if (trace != nullptr && etid == 0) trace[kTraceWords - 1] = global_timer_ns();   // split rows done
@@ -1086,6 +1093,28 @@ cudaError_t launch_pair(int device, int dtype, int head_dim, bool has_bias, cons
                         const CUtensorMap& tw_half, const WriteParams& p, int grid,
                         cudaStream_t stream) {
   return dispatch<true>(device, dtype, head_dim, has_bias, tx, tw_half, p, grid, stream);
+}
+
+int single_workers(int device) {
+  // CTAs of the single-CTA kernel that can be resident at once: blocks per SM
+  // (one, given its shared memory) times the SM count.  The split-tile waits
+  // assume every CTA of the grid is resident, so the grid never exceeds this.
+  static std::atomic<int> cache[64];
+  const int d = device & 63;
+  int n = cache[d].load();
+  if (n > 0) return n;
+  auto kern = ctx_kv_tiled_kernel<__nv_bfloat16, 128, false, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(tiled_smem_bytes<false>())) != cudaSuccess)
+    return 0;
+  int per_sm = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTiledThreads, tiled_smem_bytes<false>()) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || per_sm <= 0 ||
+      sms <= 0)
+    return 0;
+  cache[d].store(per_sm * sms);
+  return per_sm * sms;
 }
 
 int pair_workers(int device) {

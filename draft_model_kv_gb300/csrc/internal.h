@@ -9,6 +9,7 @@
 namespace dspark {
 
 constexpr int kMaxDpPerm = 160;   // whole tiles that a launch may reorder (one wave of SMs)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bound on any single in-kernel wait (2 s)
 
 // Everything the fused write needs besides the two operand tensor maps.
 struct WriteParams {
@@ -51,6 +52,11 @@ struct WriteParams {
   float* workspace;             // [gridDim.x][2][kTileN/4][kTileM][4] fp32 partial tiles
   int32_t* counters;            // [gridDim.x] arrivals per cut tile, reset by the last one
   uint64_t wait_limit_ns;       // bound on any single in-kernel wait
+  // waits for the parts other workers publish of a cut tile: the bound, and
+  // how many arrivals beyond the real contributors they wait for (0; more
+  // only in the timeout test, where no worker will reach the count)
+  uint64_t split_wait_ns;
+  int32_t split_wait_extra;
   int16_t dp_perm[kMaxDpPerm];
   void* k_pool[DSPARK_MAX_LAYERS];
   void* v_pool[DSPARK_MAX_LAYERS];
@@ -204,8 +210,13 @@ cudaError_t launch_plain(int device, int dtype, const CUtensorMap& tmap_x, const
 bool make_operand_map(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint64_t rows,
                       uint64_t pitch_elems, uint32_t box_rows);
 
-// Number of CTA pairs that can be resident at once on `device` (0 if unknown).
+// Workers that can be resident at once on `device` (0 if unknown): CTA pairs
+// of the pair kernel, CTAs of the single-CTA kernel, CTAs of the streaming
+// kernel with a launch's stage layout.  Grids never exceed them, since the
+// split-tile waits assume that every CTA of a grid is resident.
 int pair_workers(int device);
+int single_workers(int device);
+int stream_workers(int device, int stages, uint32_t stage_b);
 
 // Convert a [n] bf16 / fp16 / fp32 vector to fp32 (bundle packing).
 cudaError_t launch_to_fp32(const void* src, int dtype, float* dst, int n, cudaStream_t stream);

@@ -16,8 +16,13 @@
 //  - the array is kNoAllocScratchBytes (16 MiB + 4 KiB) on every GPU that loads
 //    the library, held until the process exits;
 //  - a call runs on at most kNoAllocMaxCtas (64) SMs, the number of CTAs whose
-//    partial tiles fit in the array; a launch that would need more scratch is
-//    refused with DSPARK_E_SCRATCH_LIMIT;
+//    partial tiles fit in the array.  The scratch a launch uses grows with its
+//    CTA count only, never with the token count or the model's sizes, so with
+//    this cap every problem fits; DSPARK_E_SCRATCH_LIMIT stays as a guard that
+//    valid arguments never reach;
+//  - a NULL status_flags sends the device flags (out-of-range positions or
+//    slots, a wait that ran out) to a word inside the array that no call reads
+//    back: those errors are then discarded;
 //  - every call uses the same array: two calls whose kernels overlap on the GPU
 //    (different streams without ordering, or two host threads) race and give
 //    wrong results; keep calls on one device ordered (one stream, or events);
@@ -43,6 +48,9 @@ constexpr size_t kNoAllocWorkspaceBytes = static_cast<size_t>(kNoAllocMaxCtas) *
 constexpr size_t kNoAllocCounterOffset = kNoAllocWorkspaceBytes;                 // int32 [kNoAllocMaxCtas]
 constexpr size_t kNoAllocStatusOffset = kNoAllocWorkspaceBytes + 2048;           // uint32 fallback status word
 constexpr size_t kNoAllocScratchBytes = kNoAllocWorkspaceBytes + 4096;
+static_assert(kNoAllocCounterOffset + sizeof(int32_t) * kNoAllocMaxCtas <= kNoAllocStatusOffset,
+              "arrival counters overlap the status word");
+static_assert(kNoAllocStatusOffset + sizeof(uint32_t) <= kNoAllocScratchBytes, "status word outside the array");
 
 // The scratch itself.  In host code this name is only a stand-in for the
 // device symbol: never pass it to a kernel; use the address looked up below.
@@ -177,7 +185,9 @@ extern "C" int dspark_write_ctx_kv_noalloc(
   p.num_tiles = p.num_m * p.num_n;
   const int ctas = scratch->sms < kNoAllocMaxCtas ? scratch->sms : kNoAllocMaxCtas;
   const int grid = plan_schedule(p.num_tiles, p.num_kb, ctas, true, p);
-  // the workspace this launch uses must fit in the static array
+  // plan_schedule never returns more workers than it is given, so the
+  // workspace of the launch fits (workspace_bytes(kNoAllocMaxCtas) is the
+  // array's workspace part); the check guards that rule
   if (workspace_bytes(grid) > kNoAllocWorkspaceBytes || grid > kNoAllocMaxCtas)
     return DSPARK_E_SCRATCH_LIMIT;
 
@@ -201,7 +211,9 @@ extern "C" int dspark_write_ctx_kv_noalloc(
   p.status = status_flags != nullptr ? status_flags
                                      : reinterpret_cast<uint32_t*>(scratch->base + kNoAllocStatusOffset);
   p.trace = nullptr;
-  p.wait_limit_ns = 2000000000ull;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.split_wait_ns = kWaitLimitNs;
+  p.split_wait_extra = 0;
   for (int l = 0; l < num_layers; ++l) {
     p.k_pool[l] = k_pools[l];
     p.v_pool[l] = v_pools[l];

@@ -131,7 +131,8 @@ DSPARK_API int dspark_check_ctx_kv_layers(const dspark_layer_desc* layers /* (ho
  * nothing on refusal.  The bundle is owned by the library: free it with
  * dspark_free_bundle.  It is bound to the device current at the call.  The
  * copies run on `stream` and the call synchronises that stream before it
- * returns, so the bundle is ready for use on any stream.  The bundle keeps a
+ * returns, so the bundle is ready for use on any stream (writes with one
+ * bundle must still be ordered: see dspark_write_ctx_kv).  The bundle keeps a
  * snapshot: if the model's weights change, pack again (PR #31986 page, Risks:
  * the cached stack assumes frozen weights).
  */
@@ -165,6 +166,19 @@ DSPARK_API int dspark_pack_ctx_kv(const dspark_layer_desc* layers /* (host) [num
  * a loc >= pool_slots is a caller error: that token is skipped and a device
  * status flag is set.  num_tokens == 0 returns DSPARK_OK at once.
  * Enqueues one kernel on `stream`; no host synchronisation.
+ *
+ * Concurrency.  Every write with a bundle uses that bundle's scratch: the
+ * partial tiles of the work split, their arrival counters and the status
+ * word.  Writes with the same bundle must therefore be ordered on the GPU
+ * (one stream, or streams ordered by events); two that overlap race on the
+ * scratch and write wrong values.  Writes with different bundles may overlap.
+ * The grid is sized to what the device can hold resident at once (one CTA, or
+ * CTA pair, per SM or SM pair), and a CTA may wait, bounded, for parts that
+ * other CTAs of the same launch publish.  If other work holds SMs while the
+ * write runs (a concurrent kernel, an MPS thread limit, a green context) those
+ * waits can run out: the write then stops, sets DSPARK_FLAG_TIMEOUT and leaves
+ * some rows unwritten rather than hanging; dspark_clear_device_status makes the
+ * bundle usable again.
  */
 DSPARK_API int dspark_write_ctx_kv(dspark_bundle_t bundle,
                         const void* ctx_hidden, int64_t num_tokens,
@@ -201,12 +215,19 @@ DSPARK_API int dspark_write_ctx_kv(dspark_bundle_t bundle,
  *  stacked_bias      NULL or [N] in dtype
  *  k_norm_weight     [num_layers, head_dim] fp32, 16-byte aligned
  *  dtype             DSPARK_DTYPE_BF16 or DSPARK_DTYPE_FP16 (weights, hidden, pools)
- *  status_flags      NULL, or a device uint32 the kernel ORs DSPARK_FLAG_* bits into
+ *  status_flags      a device uint32 the kernel ORs DSPARK_FLAG_* bits into, or NULL:
+ *                    then the flags (out-of-range positions or slots, a wait that ran
+ *                    out) go to a word inside the library's array that no call reads
+ *                    back, so those errors are discarded
  *  other arguments   as for dspark_write_ctx_kv
+ * The sizes of the caller's buffers are not known to this call (there is no
+ * bundle to check them against): they must match the arguments.
  *
- * A call runs on at most 64 SMs (the CTAs whose partial tiles fit in the
- * array); a launch that would need more scratch is refused with
- * DSPARK_E_SCRATCH_LIMIT.  All calls share the one array and it keeps the
+ * A call runs on at most 64 SMs, the CTAs whose partial tiles fit in the
+ * array.  The scratch a launch uses depends on its CTA count only, not on the
+ * token count or the model's sizes, so every problem fits;
+ * DSPARK_E_SCRATCH_LIMIT is a guard that valid arguments never reach.  All
+ * calls share the one array and it keeps the
  * previous call's contents: each call clears the arrival counters (a
  * stream-ordered memset) before its kernel, and two calls whose kernels
  * overlap on the GPU race and give wrong results, so keep the calls on a
@@ -230,7 +251,9 @@ DSPARK_API int dspark_write_ctx_kv_noalloc(
  * `stream`; synchronises `stream`. */
 DSPARK_API int dspark_get_device_status(dspark_bundle_t bundle, void* stream, uint32_t* flags /* (host) */);
 
-/* Reset the device status word to 0 (stream-ordered, asynchronous). */
+/* Reset the device status word to 0 and the split-tile arrival counters
+ * (stream-ordered, asynchronous).  Call it after a write that reported
+ * DSPARK_FLAG_TIMEOUT: such a write may leave counters set. */
 DSPARK_API int dspark_clear_device_status(dspark_bundle_t bundle, void* stream);
 
 /* Kernel variant used by later writes with this bundle.
@@ -257,6 +280,19 @@ DSPARK_API int dspark_set_kernel_variant(dspark_bundle_t bundle, int32_t variant
  * is the buffer length; NULL turns tracing off (the default).  Tracing adds a
  * few global stores per work item and does not change results. */
 DSPARK_API int dspark_set_trace_buffer(dspark_bundle_t bundle, uint64_t* buf, int64_t words);
+
+/* Diagnostics for tests of the timeout path: later writes with this bundle
+ * wait for `missing_arrivals` more published parts of every tile that is cut
+ * between CTAs than there are contributors (a count that no CTA will reach),
+ * and give up on each such wait after `limit_ns` nanoseconds (1 .. 2e9)
+ * instead of the normal 2 s.  Those waits then run out: the write stops,
+ * sets DSPARK_FLAG_TIMEOUT and returns with the rows of those tiles (and
+ * possibly others) unwritten.  Every other wait keeps its normal bound, and
+ * each CTA still waits for its own copies and tensor-core work before it
+ * exits, so the GPU stays usable.  A write without cut tiles is unaffected.
+ * missing_arrivals = 0 restores normal writes.  Returns DSPARK_E_INVALID_ARG
+ * for a negative count, more than 1024, or a limit outside 1 .. 2e9 ns. */
+DSPARK_API int dspark_set_split_wait_test(dspark_bundle_t bundle, int32_t missing_arrivals, uint64_t limit_ns);
 
 DSPARK_API int dspark_bundle_get_info(dspark_bundle_t bundle, dspark_bundle_info* info /* (host) */);
 
