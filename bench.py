@@ -236,6 +236,7 @@ def run_gpu(args, w):
     _build.build()
     st = stage(w, device=f"cuda:{local}")
     bundle = dk.dspark_pack_ctx_kv(st["layers"], w.H)
+    dk.dspark_set_kernel_variant(bundle, args.variant)
     for lay in st["layers"]:          # the bundle holds its own copy of the K|V rows
         lay.qkv_weight = None
     torch.cuda.empty_cache()
@@ -342,7 +343,7 @@ def run_gpu(args, w):
         "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "fp16", "data": "synthetic",
-        "config": config_of(w),
+        "config": dict(config_of(w), variant=args.variant),
         "roofline": roof_tc if bound == "tensor" else roof_hbm,
         "roofline_other": roof_hbm if bound == "tensor" else roof_tc,
         "roofline_time_frac": max(t_tc, t_hbm) / (mean_ms * 1e-3),
@@ -873,6 +874,7 @@ def run_trace(args, w):
     _build.build()
     st = stage(w, device="cuda")
     bundle = dk.dspark_pack_ctx_kv(st["layers"], w.H)
+    dk.dspark_set_kernel_variant(bundle, args.variant)
     pools = dk.dspark_bind_pools(bundle, st["k_pools"], st["v_pools"])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -935,6 +937,8 @@ def main(argv=None):
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", default="auto", choices=["auto", "single", "pair", "stream"],
+                    help="kernel of the write (dspark_set_kernel_variant); auto picks by token count")
     ap.add_argument("--trace", action="store_true",
                     help="print per-CTA timelines of --steps traced writes instead of a bench line")
     ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify", "attention", "combine"],
