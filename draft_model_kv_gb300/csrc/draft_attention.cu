@@ -2,21 +2,29 @@
 // K3 DSpark draft attention: GQA, non-causal, the context gathered from the
 // pool through kv_indices, split over the context and merged).
 //
-// Stage 1 (one CTA per request and context split): the CTA holds the
-// request's queries of every KV head in shared memory and streams its share
-// of the context (then, for split 0, the block's own keys) in chunks of 16
-// tokens: each token's pool row (all KV heads, contiguous) is copied with
-// 16-byte asynchronous copies into a double-buffered stage, 16-byte units
-// XOR-swizzled by row so that the ldmatrix reads below are conflict-free.
-// Each warp owns 16 query rows of one KV head (rows = block x group, row
-// i*group + hh is query i of head g*group + hh) and runs the flash-attention
-// recurrence on the tensor cores (mma.sync m16n8k16: the rows are too few for
-// a 128-row tcgen05 tile, and the stream of gathered 256-byte rows, not the
-// MMA, bounds the kernel): S = Q K^T, online softmax in the log2 domain with
-// the running max and sum in registers, O += P V with P re-packed from the S
-// accumulators.  It writes its unnormalised O, max and sum to the workspace.
-// Stage 2 merges the splits of each query row with the log-sum-exp weights and
-// stores the output in the model dtype.
+// Stage 1 runs on the tcgen05 tensor cores, one CTA per (KV head, context
+// split, request).  For KV head g the query rows (row r = i*group + hh: query i
+// of the block, head g*group + hh) are at most 32, too few for an MMA's M, so
+// the keys take the M side:
+//
+//   S^T[key][row]  = K_g[key] . Q_g[row]            M = 128 keys, N = rows, K = D
+//   O^T[d][row]   += V_g^T[d][key] . P^T[row][key]  M = 128 (d), N = rows, K = 128 keys
+//
+// both accumulated in TMEM (S double-buffered).  Four producer warps gather,
+// per 128-key chunk, each key's 2 x D x 2 bytes of head g (its K and V rows of
+// the pool, or of the block's own keys for the last chunk of split 0) with
+// 16-byte asynchronous copies into the 128-byte-swizzled layout of the MMA
+// operands, three stages deep; the staged chunk is the K-major A operand of
+// the first product and, read as an MN-major operand, the V^T of the second.
+// Four softmax warps own one key (TMEM lane) each: they load the key's scores
+// for every query row, take the per-row maximum and sum over the 128 keys with
+// warp transpose-reductions, run the online softmax in the log2 domain, write
+// P^T (model dtype) to shared memory as the B operand of the second product
+// and rescale O^T in TMEM when a row's maximum grows by more than 2^8 (so the
+// softmax seldom waits for the previous product).  One thread issues the
+// MMAs.  Each split writes its unnormalised O, maximum and sum to the
+// workspace; stage 2 merges the splits of each query row with the
+// log-sum-exp weights and stores the output in the model dtype.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -24,52 +32,55 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "../../include/dspark_attention.h"
+#include "ptx.cuh"
 
 namespace dspark {
 namespace {
 
-constexpr int kChunk = 16;               // keys per pipeline stage
-constexpr int kMaxSplitTokens = 2048;    // context tokens per split at most
+constexpr int kKeys = 128;               // keys per chunk: the first product's M (TMEM lanes)
+constexpr int kQRows = 32;               // query rows per KV head, at most (TMEM columns per accumulator)
+constexpr int kAttnStages = 3;           // chunks in the operand ring
+constexpr int kSoftThreads = 128;        // warps 0-3: softmax, one key / TMEM lane each
+constexpr int kProdThreads = 128;        // warps 4-7: producers, one key each
+constexpr int kAttnMmaWarp = 8;
+constexpr int kAttnThreads = 9 * 32;
+constexpr int kSplitGoal = 2048;         // context tokens per split aimed for
+constexpr int kMaxSplitTokens = 8192;
 constexpr int kWaveCtas = 152;           // stage-1 CTAs resident at once (one per SM of a GB300)
-constexpr int kSplitGoal = 1024;         // context tokens per split aimed for
-constexpr int kMaxWarps = 16;
 constexpr int kCombineWarps = 8;
+constexpr uint32_t kAttnTmemCols = 128;  // S0 at column 0, S1 at 32, O at 64
+constexpr uint64_t kAttnWaitNs = 2000000000ull;
+// A row's running maximum (log2 domain) is raised, and O and the sum
+// rescaled, only when a chunk's maximum exceeds it by more than this: the
+// weights stay below 2^8 (exact enough in the model dtype), and O seldom needs
+// the previous chunk's product to be complete.
+constexpr float kLazyRescale = 8.f;
 
 struct AttnPlan {
   int splits;
   int split_tokens;
 };
 
-// Context split: about kSplitGoal tokens per split, at least two waves of
-// CTAs (more splits cost workspace traffic and merge work: measured slower),
-// and among up to twice that many splits the count whose CTAs fill the last
-// wave best (a request's unused splits end at once, so this matters for
-// equal context lengths).  Depends on the sizes only, so the workspace size
-// query and the launch agree.
-AttnPlan make_plan(int64_t batch, int64_t max_context) {
+// Context split: about kSplitGoal tokens per split (a multiple of the chunk),
+// and more, shorter splits when batch x KV heads CTAs per split would not
+// fill two waves.  Depends on the sizes only, so the workspace size query and
+// the launch agree.
+AttnPlan make_plan(int64_t batch, int nkv, int64_t max_context) {
   AttnPlan pl;
   if (batch < 1) batch = 1;
-  int64_t base = (max_context + kSplitGoal - 1) / kSplitGoal;
-  const int64_t waves2 = (2 * kWaveCtas + batch - 1) / batch;
-  if (base < waves2) base = waves2;
-  if (base < 1) base = 1;
-  int64_t best = base;
-  double best_eff = 0.0;
-  for (int64_t sp = base; sp <= 2 * base; ++sp) {
-    const int64_t ctas = batch * sp;
-    const double eff = static_cast<double>(ctas) / (((ctas + kWaveCtas - 1) / kWaveCtas) * kWaveCtas);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
-      best = sp;
-    }
-  }
-  int64_t c = (max_context + best - 1) / best;
-  c = (c + kChunk - 1) / kChunk * kChunk;
-  if (c < kChunk) c = kChunk;
+  int64_t splits = (max_context + kSplitGoal - 1) / kSplitGoal;
+  const int64_t per_split = batch * nkv;
+  const int64_t want = (2 * kWaveCtas + per_split - 1) / per_split;
+  if (splits < want) splits = want;
+  if (splits < 1) splits = 1;
+  int64_t c = (max_context + splits - 1) / splits;
+  c = (c + kKeys - 1) / kKeys * kKeys;
+  if (c < kKeys) c = kKeys;
   if (c > kMaxSplitTokens) c = kMaxSplitTokens;
-  int64_t splits = (max_context + c - 1) / c;
+  splits = (max_context + c - 1) / c;
   if (splits < 1) splits = 1;
   pl.splits = static_cast<int>(splits);
   pl.split_tokens = static_cast<int>(c);
@@ -87,6 +98,7 @@ struct AttnParams {
   const int64_t* kv_indices;
   const int64_t* kv_start;
   int64_t batch;
+  int64_t max_context;   // longer contexts are cut here (and flagged)
   int block, nq, nkv, group, rows, splits, split_tokens;
   float scale_log2;
   void* out;
@@ -96,316 +108,463 @@ struct AttnParams {
 };
 
 template <typename E>
-struct MmaOps;
-
+__device__ __forceinline__ uint16_t to_bits(float v);
 template <>
-struct MmaOps<__nv_bfloat16> {
-  __device__ static __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-  __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    uint32_t u;
-    memcpy(&u, &h, 4);
-    return u;
-  }
-  __device__ static __forceinline__ uint16_t one(float v) {
-    __nv_bfloat16 h = __float2bfloat16_rn(v);
-    uint16_t u;
-    memcpy(&u, &h, 2);
-    return u;
-  }
+__device__ __forceinline__ uint16_t to_bits<__nv_bfloat16>(float v) {
+  __nv_bfloat16 h = __float2bfloat16_rn(v);
+  uint16_t u;
+  memcpy(&u, &h, 2);
+  return u;
+}
+template <>
+__device__ __forceinline__ uint16_t to_bits<__half>(float v) {
+  __half h = __float2half_rn(v);
+  uint16_t u;
+  memcpy(&u, &h, 2);
+  return u;
+}
+template <typename E>
+constexpr uint32_t ab_format() {
+  return std::is_same<E, __nv_bfloat16>::value ? 1u : 0u;
+}
+
+// Shared memory of stage 1 (byte offsets from a 1024-byte aligned base).  A
+// staged chunk is K then V of head g, each [D/64 blocks][128 keys][128 B]
+// (64 columns of a key per 128-byte row, 16-byte units XOR-swizzled by key).
+struct AttnLayout {
+  uint32_t stage_bytes, v_off, q_off, p_off, red_off, bar_off, total;
 };
 
-template <>
-struct MmaOps<__half> {
-  __device__ static __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-  __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    uint32_t u;
-    memcpy(&u, &h, 4);
-    return u;
-  }
-  __device__ static __forceinline__ uint16_t one(float v) {
-    __half h = __float2half_rn(v);
-    uint16_t u;
-    memcpy(&u, &h, 2);
-    return u;
-  }
+__host__ __device__ inline AttnLayout attn_layout(int D) {
+  AttnLayout L;
+  const uint32_t blk = kKeys * 128;                        // 64 columns of 128 keys: 16 KB
+  L.v_off = static_cast<uint32_t>(D / 64) * blk;
+  L.stage_bytes = 2 * L.v_off;
+  L.q_off = kAttnStages * L.stage_bytes;                   // Q: [D/64][32 rows][128 B]
+  L.p_off = L.q_off + static_cast<uint32_t>(D / 64) * kQRows * 128;   // P^T: 2 x [2][32 rows][128 B]
+  L.red_off = L.p_off + 2 * 2 * kQRows * 128;
+  L.bar_off = L.red_off + 2048;
+  L.total = L.bar_off + 256 + 1024;                        // + alignment slack
+  return L;
+}
+
+struct AttnBarriers {
+  uint64_t full[kAttnStages];
+  uint64_t empty[kAttnStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];   // the O product of chunk c, per P buffer c & 1
+  uint64_t q_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int rescale;     // some row's maximum grew in this chunk (O must be rescaled)
 };
+static_assert(sizeof(AttnBarriers) <= 256, "barrier area");
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+// Shared-memory matrix descriptor of an MN-major operand in the 128-byte
+// swizzle layout: 64 consecutive M elements per 128-byte row, 8 rows (K) per
+// 1024-byte atom, atoms `lbo` bytes apart along M and 1024 bytes apart along
+// K.  Descriptor version 1, layout type 2 (SWIZZLE_128B).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+// Transpose-reduction over a warp: on entry lane l holds v[j] = value of
+// (row l, column j); on exit v[0] of lane l is the reduction over the 32 rows
+// of column l.
+template <bool kMax>
+__device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      const float other = __shfl_xor_sync(0xffffffffu, send, off);
+      v[i] = kMax ? fmaxf(keep, other) : keep + other;
+    }
+  }
+  return v[0];
 }
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+__device__ __forceinline__ void attn_flag(const AttnParams& p, uint32_t bits) {
+  if (p.status != nullptr) atomicOr(p.status, bits);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
-__device__ __forceinline__ void cp_async_wait() {
+__device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-
-// Shared memory of stage 1 (byte offsets from a 128-byte aligned base).
-struct AttnSmem {
-  uint32_t q_off, kv_off, valid_off, idx_off, stage_bytes, row_bytes, total;
-};
-
-__host__ __device__ inline AttnSmem attn_smem(int D, int nkv, int rows, int split_tokens) {
-  AttnSmem s;
-  s.row_bytes = static_cast<uint32_t>(nkv * D * 2);                   // one token's pool row, all KV heads
-  s.q_off = 0;
-  s.kv_off = static_cast<uint32_t>(nkv * rows * D * 2);              // Q of every KV head
-  s.stage_bytes = 2 * kChunk * s.row_bytes;                            // K then V rows of one chunk
-  s.valid_off = s.kv_off + 2 * s.stage_bytes;
-  s.idx_off = s.valid_off + 2 * kChunk * 4;
-  s.total = s.idx_off + static_cast<uint32_t>(split_tokens) * 8;
-  return s;
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 template <typename E, int D>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) attn_split_kernel(const AttnParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int kUnitsD = D / 8;                 // 16-byte units of one head row
-  const int nkv = p.nkv, rows = p.rows;
-  const AttnSmem L = attn_smem(D, nkv, rows, p.split_tokens);
-  const int units_row = nkv * kUnitsD;           // 16-byte units of one token's pool row
-  uint8_t* q_s = smem + L.q_off;
-  uint8_t* kv_s = smem + L.kv_off;
-  int* valid_s = reinterpret_cast<int*>(smem + L.valid_off);
-  int64_t* idx_s = reinterpret_cast<int64_t*>(smem + L.idx_off);
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const AttnLayout L = attn_layout(D);
+  AttnBarriers* bars = reinterpret_cast<AttnBarriers*>(smem + L.bar_off);
+  float* red_max = reinterpret_cast<float*>(smem + L.red_off);          // [4][32]
+  float* red_sum = red_max + 4 * 32;                                     // [4][32]
+  float* m_new = red_sum + 4 * 32;                                       // [32]
+  float* alpha_s = m_new + 32;                                           // [32]
+  volatile int* abort_flag = &bars->abort;
+  constexpr int kBlocksD = D / 64;
 
-  const int tid = threadIdx.x, nthreads = blockDim.x;
-  const int warp = tid / 32, lane = tid % 32;
-  const int64_t b = blockIdx.y;
-  const int s = blockIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // the KV heads of one (request, split) are adjacent CTAs, so that the
+  // pieces they read of the same pool rows are requested close in time
+  const int64_t b = blockIdx.z;
+  const int g = blockIdx.x;
+  const int s = blockIdx.y;
   const int64_t k0 = p.kv_start[b];
   int64_t n_b = p.kv_start[b + 1] - k0;
-  const int64_t cap = static_cast<int64_t>(p.splits) * p.split_tokens;
-  if (n_b > cap) {
-    if (s == 0 && tid == 0 && p.status != nullptr) atomicOr(p.status, DSPARK_FLAG_CONTEXT_RANGE);
-    n_b = cap;
+  if (n_b > p.max_context) {
+    if (s == 0 && g == 0 && threadIdx.x == 0) attn_flag(p, DSPARK_FLAG_CONTEXT_RANGE);
+    n_b = p.max_context;
   }
   if (n_b < 0) n_b = 0;
+  if (p.pool_slots <= 0 && n_b > 0) {   // an empty pool: every context key is out of range
+    if (s == 0 && g == 0 && threadIdx.x == 0) attn_flag(p, DSPARK_FLAG_LOC_RANGE);
+    n_b = 0;
+  }
   const int64_t lo = static_cast<int64_t>(s) * p.split_tokens;
   const int64_t hi = lo + p.split_tokens < n_b ? lo + p.split_tokens : n_b;
   const int n_ctx = hi > lo ? static_cast<int>(hi - lo) : 0;
   const bool has_ext = s == 0;
   if (!has_ext && n_ctx == 0) return;            // nothing in this split (uniform)
+  const int ctx_chunks = (n_ctx + kKeys - 1) / kKeys;
+  const int n_chunks = ctx_chunks + (has_ext ? 1 : 0);
 
-  for (int t = tid; t < n_ctx; t += nthreads) idx_s[t] = p.kv_indices[k0 + lo + t];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kAttnStages; ++i) {
+      mbar_init(smem_u32(&bars->full[i]), kProdThreads);
+      mbar_init(smem_u32(&bars->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->s_full[i]), 1);
+      mbar_init(smem_u32(&bars->s_free[i]), kSoftThreads / 32);
+      mbar_init(smem_u32(&bars->p_full[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->pv_done[0]), 1);
+    mbar_init(smem_u32(&bars->pv_done[1]), 1);
+    mbar_init(smem_u32(&bars->q_full), kProdThreads);
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    bars->rescale = 0;
+    fence_barrier_init();
+  }
+  if (warp == kAttnMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kAttnTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
 
-  const int ext_chunks = has_ext ? (p.block + kChunk - 1) / kChunk : 0;
-  const int total_chunks = ext_chunks + (n_ctx + kChunk - 1) / kChunk;
-
-  // queries of every KV head: smem row g*rows + r holds query i = r / group of
-  // head g*group + r % group
-  {
+  if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ producers
+    const int pt = threadIdx.x - kSoftThreads;   // 0..127 among the producers
+    const int pw = pt / 32;                         // producer warp
     const E* q = static_cast<const E*>(p.q);
-    const int nunits = nkv * rows * kUnitsD;
-    for (int x = tid; x < nunits; x += nthreads) {
-      const int row = x / kUnitsD, u = x % kUnitsD;
-      const int g = row / rows, r = row % rows;
-      const int i = r / p.group, hh = r % p.group;
-      const E* src = q + ((b * p.block + i) * p.nq + g * p.group + hh) * D + u * 8;
-      cp_async16(smem_addr(q_s + row * (D * 2) + ((u ^ (row & 7)) * 16)), src);
+    // Q of head g: row r = i*group + hh, its D columns as D/64 128-byte rows
+    for (int x = pt; x < p.rows * (D / 8); x += kProdThreads) {
+      const int r = x / (D / 8), u = x % (D / 8);
+      const E* src = q + ((b * p.block + r / p.group) * p.nq + g * p.group + r % p.group) * D + u * 8;
+      const uint32_t dst = smem_u32(smem + L.q_off) + (u / 8) * (kQRows * 128) + r * 128 + (((u % 8) ^ (r & 7)) * 16);
+      cp_async16(dst, src);
     }
-  }
-
-  const bool units_fixed = nthreads % units_row == 0;
-  const int my_u = tid % units_row, my_j0 = tid / units_row, j_step = nthreads / units_row;
-  auto issue = [&](int ci, int stage) {
-    uint8_t* ks = kv_s + stage * L.stage_bytes;
-    uint8_t* vs = ks + kChunk * L.row_bytes;
-    const E* kbase;
-    const E* vbase;
-    auto copy_unit = [&](int j, int u) {
-      bool ok;
-      int64_t row_off;
-      if (ci < ext_chunks) {
-        const int e = ci * kChunk + j;
-        ok = e < p.block;
-        row_off = (b * p.block + e) * static_cast<int64_t>(nkv) * D;
-        kbase = static_cast<const E*>(p.k_ext);
-        vbase = static_cast<const E*>(p.v_ext);
-      } else {
-        const int t = (ci - ext_chunks) * kChunk + j;
-        ok = t < n_ctx;
-        const int64_t slot = ok ? idx_s[t] : 0;
-        if (ok && (slot < 0 || slot >= p.pool_slots)) {
+    cp_async_commit_group();
+    bool ok_run = true;
+    for (int c = 0; c < n_chunks && ok_run; ++c) {
+      const int st = c % kAttnStages;
+      if (c >= kAttnStages &&
+          !mbar_wait(smem_u32(&bars->empty[st]), static_cast<uint32_t>(c / kAttnStages - 1) & 1u, abort_flag,
+                     kAttnWaitNs)) {
+        ok_run = false;
+        break;
+      }
+      // Warp pw copies keys 32*pw .. 32*pw+31 of the chunk.  Lane l learns the
+      // slot of key 32*pw + l; then the warp copies its keys one (D = 128) or
+      // two (D = 64) at a time, the lanes taking consecutive 16-byte units of
+      // the key's K row and then its V row, so that every copy instruction
+      // reads whole contiguous row segments.
+      int64_t my_k, my_v;   // element offsets of this lane's key's rows (K pool / K ext space)
+      bool my_ok;
+      {
+        const int key = 32 * pw + lane;
+        if (c < ctx_chunks) {
+          const int64_t t = lo + static_cast<int64_t>(c) * kKeys + key;
+          my_ok = t < hi;
+          int64_t slot = my_ok ? p.kv_indices[k0 + t] : 0;
+          if (my_ok && (slot < 0 || slot >= p.pool_slots)) {
+            attn_flag(p, DSPARK_FLAG_LOC_RANGE);
+            my_ok = false;
+          }
+          if (!my_ok) slot = 0;
+          my_k = my_v = slot * p.pool_row_stride + g * D;
+        } else {
+          my_ok = key < p.block;
+          const int64_t row = b * p.block + (my_ok ? key : 0);
+          my_k = my_v = (row * p.nkv + g) * D;
+        }
+      }
+      const E* kbase = static_cast<const E*>(c < ctx_chunks ? p.k_pool : p.k_ext);
+      const E* vbase = static_cast<const E*>(c < ctx_chunks ? p.v_pool : p.v_ext);
+      uint8_t* kst = smem + st * L.stage_bytes;
+      constexpr int kUnits = D / 8;                 // 16-byte units of one head row
+      constexpr int kPerIter = 32 / (2 * kUnits);   // keys per warp instruction
+      const int sub = lane / (2 * kUnits), w = lane % (2 * kUnits);
+      const bool is_v = w >= kUnits;
+      const int u = is_v ? w - kUnits : w;
+#pragma unroll 4
+      for (int j = 0; j < 32; j += kPerIter) {
+        const int kl = j + sub;                     // key within the warp's 32
+        const int key = 32 * pw + kl;
+        const bool ok = __shfl_sync(0xffffffffu, my_ok, kl);
+        const int64_t off = __shfl_sync(0xffffffffu, is_v ? my_v : my_k, kl);
+        const uint32_t dst_off = (is_v ? L.v_off : 0u) + (u / 8) * (kKeys * 128) + key * 128 +
+                                 (((u % 8) ^ (key & 7)) * 16);
+        if (ok)
+          cp_async16(smem_u32(kst + dst_off), (is_v ? vbase : kbase) + off + u * 8);
+        else
+          // a masked key: finite zeros (its weight is 0, and 0 x NaN would not be)
+          *reinterpret_cast<uint4*>(kst + dst_off) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      cp_async_commit_group();
+      // the previous group (Q for c = 0, else chunk c-1) has landed: make it
+      // visible to the tensor cores and release it
+      cp_async_wait_group<1>();
+      fence_proxy_async_smem();
+      if (c == 0)
+        mbar_arrive(smem_u32(&bars->q_full));
+      else
+        mbar_arrive(smem_u32(&bars->full[(c - 1) % kAttnStages]));
+    }
+    cp_async_wait_group<0>();
+    fence_proxy_async_smem();
+    if (ok_run) {
+      if (n_chunks == 0) mbar_arrive(smem_u32(&bars->q_full));
+      else mbar_arrive(smem_u32(&bars->full[(n_chunks - 1) % kAttnStages]));
+    } else if (threadIdx.x == kSoftThreads) {
+      *abort_flag = 1;
+      attn_flag(p, DSPARK_FLAG_TIMEOUT);
+    }
+  } else if (warp == kAttnMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = f16_instr_desc(ab_format<E>(), kKeys, p.rows);
+      const uint32_t idesc_pv = f16_instr_desc(ab_format<E>(), kKeys, p.rows) | (1u << 15);   // A MN-major
+      const uint32_t q_addr = smem_u32(smem + L.q_off);
+      const uint32_t p_addr = smem_u32(smem + L.p_off);
+      const uint32_t t_o = tmem_base + 2 * kQRows;
+      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, kAttnWaitNs);
+      bool issued = false;
+      auto issue_pv = [&](int j) -> bool {
+        if (!mbar_wait(smem_u32(&bars->p_full[j & 1]), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
+                       kAttnWaitNs))
+          return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + (j % kAttnStages) * L.stage_bytes + L.v_off);
+        const uint32_t pb = p_addr + (j & 1) * (2 * kQRows * 128);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          // 16 keys: two 8-key groups of the V block (1024 bytes each); P^T
+          // rows hold 64 keys per 128-byte block
+          const uint64_t ad = sw128_mnmajor_desc(v_addr + kk * 2048, D == 128 ? kKeys * 128 : 0);
+          const uint64_t bd = sw128_kmajor_desc(pb + (kk / 4) * (kQRows * 128) + (kk % 4) * 32);
+          umma_f16(t_o, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&bars->empty[j % kAttnStages]));
+        umma_commit(smem_u32(&bars->pv_done[j & 1]));
+        issued = true;
+        return true;
+      };
+      // The product of chunk c - 1 goes first: it releases that chunk's stage
+      // as soon as its softmax is done; the scores of chunk c follow once it
+      // has landed (the softmax warps reach chunk c only after chunk c - 1).
+      for (int c = 0; c < n_chunks && ok; ++c) {
+        if (c >= 1 && !issue_pv(c - 1)) {
           ok = false;
-          if (u == 0 && p.status != nullptr) atomicOr(p.status, DSPARK_FLAG_LOC_RANGE);
+          break;
         }
-        row_off = slot * p.pool_row_stride;
-        kbase = static_cast<const E*>(p.k_pool);
-        vbase = static_cast<const E*>(p.v_pool);
+        const int st = c % kAttnStages;
+        if (!mbar_wait(smem_u32(&bars->full[st]), static_cast<uint32_t>(c / kAttnStages) & 1u, abort_flag,
+                       kAttnWaitNs) ||
+            (c >= 2 && !mbar_wait(smem_u32(&bars->s_free[c & 1]), static_cast<uint32_t>((c >> 1) - 1) & 1u,
+                                  abort_flag, kAttnWaitNs))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + st * L.stage_bytes);
+        const uint32_t t_s = tmem_base + (c & 1) * kQRows;
+#pragma unroll
+        for (int blk = 0; blk < kBlocksD; ++blk)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_f16(t_s, sw128_kmajor_desc(k_addr + blk * (kKeys * 128) + k * 32),
+                     sw128_kmajor_desc(q_addr + blk * (kQRows * 128) + k * 32), idesc_s,
+                     (blk != 0 || k != 0) ? 1u : 0u);
+        issued = true;
+        umma_commit(smem_u32(&bars->s_full[c & 1]));
       }
-      const uint32_t off = j * L.row_bytes + ((u ^ (j & 7)) * 16);
-      if (ok) {
-        cp_async16(smem_addr(ks + off), kbase + row_off + u * 8);
-        cp_async16(smem_addr(vs + off), vbase + row_off + u * 8);
+      if (ok && n_chunks > 0) ok = issue_pv(n_chunks - 1);
+      if (!ok) {
+        *abort_flag = 1;
+        attn_flag(p, DSPARK_FLAG_TIMEOUT);
+      }
+      if (issued) {
+        umma_commit(smem_u32(&bars->drain));
+        int never = 0;
+        mbar_wait(smem_u32(&bars->drain), 0, &never, kAttnWaitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int k = threadIdx.x;                       // key of the chunk = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_o = tmem_base + lane_off + 2 * kQRows;
+    float m_run = -INFINITY, l_run = 0.f;            // warp 0, lane r: query row r
+    uint8_t* p_smem = smem + L.p_off;
+    bool done_ok = true;
+    for (int c = 0; c < n_chunks; ++c) {
+      const bool got = mbar_wait(smem_u32(&bars->s_full[c & 1]), static_cast<uint32_t>(c >> 1) & 1u, abort_flag,
+                                 kAttnWaitNs);
+      if (!named_barrier_and(1, kSoftThreads, got)) {
+        done_ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sraw[32];
+      tmem_ld32(tmem_base + lane_off + (c & 1) * kQRows, sraw);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[c & 1]));
+      bool valid;
+      if (c < ctx_chunks) {
+        const int64_t t = lo + static_cast<int64_t>(c) * kKeys + k;
+        valid = t < hi;
+        if (valid) {
+          const int64_t slot = p.kv_indices[k0 + t];
+          valid = slot >= 0 && slot < p.pool_slots;
+        }
       } else {
-        *reinterpret_cast<uint4*>(ks + off) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(vs + off) = make_uint4(0u, 0u, 0u, 0u);
+        valid = k < p.block;
       }
-      if (u == 0) valid_s[stage * kChunk + j] = ok ? 1 : 0;
-    };
-    if (units_fixed) {
-      // the usual case: each thread copies one fixed 16-byte unit of every
-      // j_step-th token row (no integer division per unit)
-      for (int j = my_j0; j < kChunk; j += j_step) copy_unit(j, my_u);
-    } else {
-      for (int x = tid; x < kChunk * units_row; x += nthreads) copy_unit(x / units_row, x % units_row);
-    }
-    cp_async_commit();
-  };
-
-  // this warp: 16 query rows (mt) of KV head g
-  const int tiles_per_head = rows / 16;
-  const int g = warp / tiles_per_head, mt = warp % tiles_per_head;
-  const bool active = warp < nkv * tiles_per_head;
-  const int grp = lane / 4, tig = lane % 4;
-  float acc[D / 8][4];
+      float x[32];
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  issue(0, 0);
-  for (int ci = 0; ci < total_chunks; ++ci) {
-    const int stage = ci & 1;
-    if (ci + 1 < total_chunks) {
-      issue(ci + 1, stage ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    if (active) {
-      const uint8_t* ks = kv_s + stage * L.stage_bytes;
-      const uint8_t* vs = ks + kChunk * L.row_bytes;
-      // ---- S = Q K^T for 16 keys
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const int mi = lane / 8;
-      const int qrow = g * rows + mt * 16 + (mi & 1) * 8 + lane % 8;
-      const int key_b = (mi >> 1) * 8 + lane % 8;
+      for (int r = 0; r < 32; ++r) x[r] = (valid && r < p.rows) ? __uint_as_float(sraw[r]) * p.scale_log2 : -INFINITY;
+      {
+        float t[32];
 #pragma unroll
-      for (int ks16 = 0; ks16 < D / 16; ++ks16) {
-        uint32_t a[4];
-        const int qu = 2 * ks16 + (mi >> 1);
-        ldsm_x4(smem_addr(q_s + qrow * (D * 2) + ((qu ^ (qrow & 7)) * 16)), a[0], a[1], a[2], a[3]);
-        uint32_t b0, b1, b2, b3;
-        const int ku = g * kUnitsD + 2 * ks16 + (mi & 1);
-        ldsm_x4(smem_addr(ks + key_b * L.row_bytes + ((ku ^ (key_b & 7)) * 16)), b0, b1, b2, b3);
-        MmaOps<E>::mma(sc[0], a, b0, b1);
-        MmaOps<E>::mma(sc[1], a, b2, b3);
+        for (int r = 0; r < 32; ++r) t[r] = x[r];
+        red_max[warp * 32 + lane] = warp_columns<true>(t, lane);
       }
-      // ---- online softmax (log2 domain); masked keys get -inf
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      named_barrier(1, kSoftThreads);
+      if (warp == 0) {
+        float cm = red_max[lane];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int2 vk = *reinterpret_cast<const int2*>(valid_s + stage * kChunk + nt * 8 + 2 * tig);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const bool ok = (e == 0 ? vk.x : vk.y) != 0;
-          sc[nt][e] = ok ? sc[nt][e] * p.scale_log2 : -INFINITY;
-          sc[nt][2 + e] = ok ? sc[nt][2 + e] * p.scale_log2 : -INFINITY;
-          mx0 = fmaxf(mx0, sc[nt][e]);
-          mx1 = fmaxf(mx1, sc[nt][2 + e]);
+        for (int w = 1; w < 4; ++w) cm = fmaxf(cm, red_max[w * 32 + lane]);
+        float al = 1.f;
+        if (cm > m_run + kLazyRescale) {   // also the first finite maximum (m_run = -inf)
+          al = m_run == -INFINITY ? 1.f : exp2f(m_run - cm);
+          m_run = cm;
         }
+        m_new[lane] = m_run;
+        alpha_s[lane] = al;
+        const bool grow = __any_sync(0xffffffffu, al != 1.f);
+        if (lane == 0) bars->rescale = grow ? 1 : 0;
       }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float al0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
-      const float al1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
-      m0 = n0;
-      m1 = n1;
-      float pr[2][4];
+      named_barrier(1, kSoftThreads);
+      const bool rescale = bars->rescale != 0;
+      float pr[32];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          pr[nt][e] = n0 == -INFINITY ? 0.f : exp2f(sc[nt][e] - n0);
-          pr[nt][2 + e] = n1 == -INFINITY ? 0.f : exp2f(sc[nt][2 + e] - n1);
-        }
+      for (int r = 0; r < 32; ++r) {
+        const float mr = m_new[r];
+        pr[r] = (x[r] == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(x[r] - mr);
       }
-      l0 = l0 * al0 + pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
-      l1 = l1 * al1 + pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
-      // the running max of a row seldom changes after the first chunks: skip
-      // the multiply by exactly 1
-      if (al0 != 1.f || al1 != 1.f) {
+      // P buffer c & 1 was read by the product of chunk c - 2
+      bool pv_ok = c < 2 || mbar_wait(smem_u32(&bars->pv_done[c & 1]), static_cast<uint32_t>((c >> 1) - 1) & 1u,
+                                      abort_flag, kAttnWaitNs);
+      // P^T[row][key] in the model dtype: row r of block k/64, 16-byte unit
+      // (k%64)/8 XOR-swizzled by the row
+      uint8_t* pb = p_smem + (c & 1) * (2 * kQRows * 128) + (k / 64) * (kQRows * 128) + (k % 8) * 2;
+      if (pv_ok) {
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          acc[n][0] *= al0;
-          acc[n][1] *= al0;
-          acc[n][2] *= al1;
-          acc[n][3] *= al1;
-        }
+        for (int r = 0; r < 32; ++r)
+          *reinterpret_cast<uint16_t*>(pb + r * 128 + ((((k % 64) / 8) ^ (r & 7)) * 16)) = to_bits<E>(pr[r]);
       }
-      // ---- O += P V (P re-packed from the score accumulators)
-      uint32_t pa[4];
-      pa[0] = MmaOps<E>::pack(pr[0][0], pr[0][1]);
-      pa[1] = MmaOps<E>::pack(pr[0][2], pr[0][3]);
-      pa[2] = MmaOps<E>::pack(pr[1][0], pr[1][1]);
-      pa[3] = MmaOps<E>::pack(pr[1][2], pr[1][3]);
-      const int vkey = (mi & 1) * 8 + lane % 8;
+      red_sum[warp * 32 + lane] = warp_columns<false>(pr, lane);
+      // O is rescaled only once the previous chunk's product is complete
+      if (pv_ok && rescale && c >= 1)
+        pv_ok = mbar_wait(smem_u32(&bars->pv_done[(c - 1) & 1]), static_cast<uint32_t>((c - 1) >> 1) & 1u,
+                          abort_flag, kAttnWaitNs);
+      if (!named_barrier_and(1, kSoftThreads, pv_ok)) {
+        done_ok = false;
+        break;
+      }
+      if (warp == 0) {
+        float add = 0.f;
 #pragma unroll
-      for (int dn = 0; dn < D / 8; dn += 2) {
-        uint32_t b0, b1, b2, b3;
-        const int vu = g * kUnitsD + dn + (mi >> 1);
-        ldsm_x4_trans(smem_addr(vs + vkey * L.row_bytes + ((vu ^ (vkey & 7)) * 16)), b0, b1, b2, b3);
-        MmaOps<E>::mma(acc[dn], pa, b0, b1);
-        MmaOps<E>::mma(acc[dn + 1], pa, b2, b3);
+        for (int w = 0; w < 4; ++w) add += red_sum[w * 32 + lane];
+        l_run = l_run * alpha_s[lane] + add;
       }
+      if (c >= 1 && rescale) {
+        tc_fence_after();
+        uint32_t o[32];
+        tmem_ld32(t_o, o);
+#pragma unroll
+        for (int r = 0; r < 32; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha_s[r]);
+        tmem_st32(t_o, o);
+      }
+      fence_proxy_async_smem();   // P^T (generic stores) before the tensor cores read it
+      tc_fence_before();
+      named_barrier(1, kSoftThreads);
+      if (k == 0) mbar_arrive(smem_u32(&bars->p_full[c & 1]));
     }
-    __syncthreads();   // this stage is refilled two chunks later
+    // ---- this split's unnormalised O^T, maximum and sum of every query row
+    if (done_ok && n_chunks > 0) {
+      done_ok = mbar_wait(smem_u32(&bars->pv_done[(n_chunks - 1) & 1]),
+                          static_cast<uint32_t>((n_chunks - 1) >> 1) & 1u, abort_flag, kAttnWaitNs);
+      done_ok = named_barrier_and(1, kSoftThreads, done_ok);
+    }
+    if (done_ok) {
+      tc_fence_after();
+      uint32_t o[32];
+      tmem_ld32(t_o, o);
+      const int nrows = p.nkv * p.rows;
+      const int64_t row0 = (b * p.splits + s) * static_cast<int64_t>(nrows) + static_cast<int64_t>(g) * p.rows;
+      if (k < D) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (r < p.rows) p.ws_o[(row0 + r) * D + k] = __uint_as_float(o[r]);
+      }
+      if (warp == 0 && lane < p.rows)
+        *reinterpret_cast<float2*>(p.ws_ml + (row0 + lane) * 2) = make_float2(m_run, l_run);
+    } else if (k == 0) {
+      *abort_flag = 1;
+      attn_flag(p, DSPARK_FLAG_TIMEOUT);
+    }
   }
 
-  if (!active) return;
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const int nrows = nkv * rows;
-  const int64_t base_row = (b * p.splits + s) * static_cast<int64_t>(nrows) + g * rows + mt * 16 + grp;
-  float* o0 = p.ws_o + base_row * D;
-  float* o1 = o0 + 8 * D;
-#pragma unroll
-  for (int n = 0; n < D / 8; ++n) {
-    *reinterpret_cast<float2*>(o0 + n * 8 + 2 * tig) = make_float2(acc[n][0], acc[n][1]);
-    *reinterpret_cast<float2*>(o1 + n * 8 + 2 * tig) = make_float2(acc[n][2], acc[n][3]);
-  }
-  if (tig == 0) {
-    *reinterpret_cast<float2*>(p.ws_ml + base_row * 2) = make_float2(m0, l0);
-    *reinterpret_cast<float2*>(p.ws_ml + (base_row + 8) * 2) = make_float2(m1, l1);
-  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kAttnMmaWarp) tmem_dealloc(tmem_base, kAttnTmemCols);
 }
 
 // Stage 2: one warp per (request, query row of a KV head): merge the splits.
@@ -418,9 +577,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const 
   const int64_t b = wid / nrows;
   const int row = static_cast<int>(wid % nrows);
   int64_t n_b = p.kv_start[b + 1] - p.kv_start[b];
-  const int64_t cap = static_cast<int64_t>(p.splits) * p.split_tokens;
-  if (n_b > cap) n_b = cap;
-  if (n_b < 0) n_b = 0;
+  if (n_b > p.max_context) n_b = p.max_context;
+  if (n_b < 0 || p.pool_slots <= 0) n_b = 0;
   int n_split = static_cast<int>((n_b + p.split_tokens - 1) / p.split_tokens);
   if (n_split < 1) n_split = 1;
   const int64_t r0 = b * p.splits * static_cast<int64_t>(nrows) + row;
@@ -443,17 +601,17 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const 
   const int i = rr / p.group, hh = rr % p.group;
   uint16_t* dst = static_cast<uint16_t*>(p.out) + ((b * p.block + i) * p.nq + g * p.group + hh) * D + lane * kPer;
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) dst[k] = MmaOps<E>::one(o[k] * inv);
+  for (int k = 0; k < kPer; ++k) dst[k] = to_bits<E>(o[k] * inv);
 }
 
 template <typename E, int D>
-cudaError_t launch_attention(const AttnParams& p, int warps, cudaStream_t stream) {
-  const AttnSmem L = attn_smem(D, p.nkv, p.rows, p.split_tokens);
-  auto k1 = attn_split_kernel<E, D>;
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
+  const AttnLayout L = attn_layout(D);
+  auto k1 = attn_tc_kernel<E, D>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(p.splits), static_cast<unsigned>(p.batch));
-  k1<<<grid, warps * 32, L.total, stream>>>(p);
+  dim3 grid(static_cast<unsigned>(p.nkv), static_cast<unsigned>(p.splits), static_cast<unsigned>(p.batch));
+  k1<<<grid, kAttnThreads, L.total, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = p.batch * p.nkv * p.rows;
@@ -480,18 +638,15 @@ int sm103_attn(int device) {
 // Host-side shape checks shared by the size query and the call.  Returns a
 // dspark_status.
 int check_shape(int64_t batch, int32_t block, int32_t nq, int32_t nkv, int32_t D, int64_t max_context,
-                AttnPlan* plan, int* warps, AttnSmem* smem) {
+                AttnPlan* plan) {
   if (batch < 0 || block < 1 || nq < 1 || nkv < 1 || max_context < 0) return DSPARK_E_INVALID_ARG;
   if (D != 64 && D != 128) return DSPARK_E_HEAD_DIM;
   if (nq % nkv != 0) return DSPARK_E_SHAPE_MISMATCH;
   const int64_t rows = static_cast<int64_t>(block) * (nq / nkv);
-  if (rows % 16 != 0 || rows > 64) return DSPARK_E_SHAPE_MISMATCH;
-  const int64_t w = nkv * rows / 16;
-  if (w > kMaxWarps) return DSPARK_E_SHAPE_MISMATCH;
-  *plan = make_plan(batch > 0 ? batch : 1, max_context);
-  *warps = static_cast<int>(w);
-  *smem = attn_smem(D, nkv, static_cast<int>(rows), plan->split_tokens);
-  if (smem->total > 227u * 1024u) return DSPARK_E_SHAPE_MISMATCH;
+  if (rows != 16 && rows != 32) return DSPARK_E_SHAPE_MISMATCH;
+  if (block > kKeys) return DSPARK_E_SHAPE_MISMATCH;
+  *plan = make_plan(batch > 0 ? batch : 1, nkv, max_context);
+  if (attn_layout(D).total > 227u * 1024u) return DSPARK_E_SHAPE_MISMATCH;
   return DSPARK_OK;
 }
 
@@ -508,10 +663,7 @@ extern "C" int64_t dspark_draft_attention_workspace_bytes(int64_t batch, int32_t
                                                           int64_t max_context) {
   using namespace dspark;
   AttnPlan pl;
-  int warps;
-  AttnSmem sm;
-  if (check_shape(batch, block, num_q_heads, num_kv_heads, head_dim, max_context, &pl, &warps, &sm) != DSPARK_OK)
-    return 0;
+  if (check_shape(batch, block, num_q_heads, num_kv_heads, head_dim, max_context, &pl) != DSPARK_OK) return 0;
   return workspace_for(batch, block, num_q_heads, head_dim, pl);
 }
 
@@ -524,9 +676,7 @@ extern "C" int dspark_draft_attention(const void* q, const void* k_ext, const vo
                                       void* stream_) {
   using namespace dspark;
   AttnPlan pl;
-  int warps;
-  AttnSmem sm;
-  const int st = check_shape(batch, block, num_q_heads, num_kv_heads, head_dim, max_context, &pl, &warps, &sm);
+  const int st = check_shape(batch, block, num_q_heads, num_kv_heads, head_dim, max_context, &pl);
   if (st != DSPARK_OK) return st;
   if (dtype != DSPARK_DTYPE_BF16 && dtype != DSPARK_DTYPE_FP16) return DSPARK_E_DTYPE_MISMATCH;
   if (batch == 0) return DSPARK_OK;
@@ -539,7 +689,7 @@ extern "C" int dspark_draft_attention(const void* q, const void* k_ext, const vo
       !aligned16(out) || !aligned16(workspace) || pool_row_stride % 8 != 0)
     return DSPARK_E_ALIGNMENT;
   if (workspace_bytes < workspace_for(batch, block, num_q_heads, head_dim, pl)) return DSPARK_E_SCRATCH_LIMIT;
-  if (batch > 65535) return DSPARK_E_INVALID_ARG;   // grid y
+  if (batch > 65535 || pl.splits > 65535) return DSPARK_E_INVALID_ARG;   // grid z and y
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess || !sm103_attn(device)) return DSPARK_E_DEVICE;
 
@@ -555,6 +705,7 @@ extern "C" int dspark_draft_attention(const void* q, const void* k_ext, const vo
   p.kv_indices = kv_indices;
   p.kv_start = kv_start;
   p.batch = batch;
+  p.max_context = max_context;
   p.block = block;
   p.nq = num_q_heads;
   p.nkv = num_kv_heads;
@@ -571,10 +722,9 @@ extern "C" int dspark_draft_attention(const void* q, const void* k_ext, const vo
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   cudaError_t e;
   if (dtype == DSPARK_DTYPE_BF16)
-    e = head_dim == 128 ? launch_attention<__nv_bfloat16, 128>(p, warps, stream)
-                        : launch_attention<__nv_bfloat16, 64>(p, warps, stream);
+    e = head_dim == 128 ? launch_attention<__nv_bfloat16, 128>(p, stream)
+                        : launch_attention<__nv_bfloat16, 64>(p, stream);
   else
-    e = head_dim == 128 ? launch_attention<__half, 128>(p, warps, stream)
-                        : launch_attention<__half, 64>(p, warps, stream);
+    e = head_dim == 128 ? launch_attention<__half, 128>(p, stream) : launch_attention<__half, 64>(p, stream);
   return e == cudaSuccess ? DSPARK_OK : DSPARK_E_CUDA;
 }

@@ -14,7 +14,8 @@
  *
  * Every query sees every key (no causal mask).  The context part is split
  * into chunks processed in parallel and merged with the usual log-sum-exp
- * rescaling, through a caller-provided workspace.
+ * rescaling, through a caller-provided workspace.  The per-split products
+ * run on the tcgen05 tensor cores with the accumulators in tensor memory.
  *
  * Conventions as in dspark_ctx_kv.h (device pointers unless marked (host),
  * strides in elements, dspark_status codes, host-side argument checks,
@@ -65,9 +66,10 @@ DSPARK_API int64_t dspark_draft_attention_workspace_bytes(int64_t batch, int32_t
  *                 DSPARK_FLAG_CONTEXT_RANGE when a context exceeds max_context.
  *
  * Supported shapes: head_dim 64 or 128; num_q_heads a multiple of
- * num_kv_heads; rows per KV head (block * num_q_heads / num_kv_heads) a
- * multiple of 16 and at most 64; num_kv_heads * rows / 16 <= 32; dtype BF16
- * or FP16.  batch == 0 is a successful no-op.  Returns DSPARK_E_INVALID_ARG
+ * num_kv_heads; rows per KV head (block * num_q_heads / num_kv_heads) 16 or
+ * 32 (they are the N side of the tensor-core products; the keys, 128 per
+ * step, are the M side); block <= 128; batch <= 65535; dtype BF16 or FP16.
+ * batch == 0 is a successful no-op.  Returns DSPARK_E_INVALID_ARG
  * (NULL pointer, sizes), DSPARK_E_HEAD_DIM, DSPARK_E_SHAPE_MISMATCH (an
  * unsupported head / block combination), DSPARK_E_DTYPE_MISMATCH,
  * DSPARK_E_POOL_LAYOUT, DSPARK_E_ALIGNMENT, DSPARK_E_SCRATCH_LIMIT
