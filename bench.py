@@ -373,6 +373,7 @@ KERNEL_SOURCES = {
     "qk_norm_rope": ["qk_norm_rope.cu"],
     "attention": ["draft_attention.cu"],
     "combine": ["ctx_kv_tiled.cu", "kernel_common.cuh", "internal.h", "ptx.cuh", "combine.cu"],
+    "fused": ["ctx_kv_tiled.cu", "kernel_common.cuh", "internal.h", "ptx.cuh", "fused.cu", "api.cu"],
 }
 TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
@@ -744,6 +745,153 @@ def run_attention(args):
     return res
 
 
+FUSED_METRIC = "combine_hidden_states + ctx-KV write tokens/s (one launch: main_proj, main_norm folded, write)"
+
+
+def run_fused(args):
+    """--op fused: dspark_combine_write_ctx_kv, combine_hidden_states fused
+    into the context-KV write (3 auxiliary hidden states: aux_dim = 3 x
+    hidden).  A step is one launch from aux to the written pools.  Tensor
+    roofline: 2 x T x hidden x aux_dim + 2 x T x N x hidden FLOP; HBM: both
+    weights, aux and the written pool rows (y stays in the L2 for decode-sized
+    batches and is not counted)."""
+    import dataclasses
+    import numpy as np
+    import torch
+    import synthetic
+    import draft_model_kv_gb300 as dk
+    from draft_model_kv_gb300 import build as _build
+    from synthetic.device import bits_to_tensor, stage
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = f"cuda:{local}"
+    w = make(args)
+    cw = synthetic.make_combine_workload(args.workload, tokens=w.T)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    st = stage(w, device=dev)
+    f = dk.dspark_pack_fused_ctx_kv(bits_to_tensor(cw.weight, dt, dev), bits_to_tensor(cw.norm_weight, dt, dev),
+                                    cw.eps, st["layers"])
+    for lay in st["layers"]:
+        lay.qkv_weight = None
+    torch.cuda.empty_cache()
+    aux = bits_to_tensor(cw.aux, dt, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_written = written_rows(w)
+
+    def step(a=None, pos=None, loc=None, cl=None):
+        dk.dspark_combine_write_ctx_kv(f, aux if a is None else a, st["positions"] if pos is None else pos,
+                                       st["cos_sin"], st["cache_loc"] if loc is None else loc, st["k_pools"],
+                                       st["v_pools"], commit_lens=st["commit_lens"] if cl is None else cl,
+                                       loc_row_width=st["loc_row_width"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    dk.dspark_fused_clear_status(f)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(SLEEP_CYCLES)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    flags = dk.dspark_fused_get_status(f)
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} during the timed region")
+    per_step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    dev_s = sum(per_step_ms) / 1e3
+    value, t_max, _ = aggregate(w.T * args.steps, dev_s)
+    # end to end: the step's inputs from one pinned host buffer, the launch,
+    # the status word back
+    parts = [aux, st["positions"], st["cache_loc"]] + ([] if st["commit_lens"] is None else [st["commit_lens"]])
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, k):
+        t = parts[k]
+        n = t.numel() * t.element_size()
+        return buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+
+    for k, t in enumerate(parts):
+        view(host_buf, k).copy_(t.cpu())
+    dviews = [view(dev_buf, k) for k in range(len(parts))]
+    h2d = sum(t.numel() * t.element_size() for t in parts)
+    e2e_total, e2e_steps = 0.0, max(1, min(args.steps, 200))
+    for i in range(e2e_steps + 3):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dev_buf.copy_(host_buf, non_blocking=True)
+        step(dviews[0], dviews[1], dviews[2], dviews[3] if len(dviews) > 3 else None)
+        flags = dk.dspark_fused_get_status(f, stream)
+        t1 = time.perf_counter()
+        if i >= 3:
+            e2e_total += t1 - t0
+        if flags:
+            raise RuntimeError(f"device status flags {flags:#x} in the e2e loop")
+    e2e_value, _, _ = aggregate(w.T * e2e_steps, e2e_total)
+    if rank != 0:
+        return None
+    K = cw.n_aux * cw.hidden
+    flops = 2.0 * w.T * cw.hidden * K + 2.0 * w.T * w.N * w.H
+    bytes_ = cw.hidden * K * 2 + w.T * K * 2 + w.N * w.H * 2 + n_written * w.N * 2
+    pk = peaks()
+    mean_ms = statistics.mean(per_step_ms)
+    t_step = mean_ms * 1e-3
+    traffic, traffic_note = ncu_traffic("fused", w.name, w.T)
+    tensor = {"bound": "tensor", "achieved": flops / t_step / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+              "frac": flops / t_step / 1e12 / pk["bf16_tflops"], "traffic": traffic,
+              "traffic_source": traffic_note, "peak_source": pk["source"] + " (burst: the kernel is timed alone)"}
+    hbm = {"bound": "hbm", "achieved": bytes_ / t_step / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+           "frac": bytes_ / t_step / 1e9 / pk["hbm_gbs"], "traffic": traffic, "traffic_source": traffic_note,
+           "peak_source": pk["source"]}
+    t_tc, t_hbm = flops / (pk["bf16_tflops"] * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9)
+    primary, other = (tensor, hbm) if t_tc >= t_hbm else (hbm, tensor)
+    res = {
+        "metric": FUSED_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": dict(config_of(w), workload=f"fused/{w.name}", aux_dim=K),
+        "roofline": primary, "roofline_other": other, "roofline_time_frac": max(t_tc, t_hbm) / t_step,
+        "ms_per_step_median": statistics.median(per_step_ms),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+                "steps": e2e_steps,
+                "timing": "host wall clock per step: h2d inputs + the launch + status d2h + sync"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        rows = np.arange(min(w.T, 64))
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds / 2 or reps < 1:
+            hid = oracle.round_to(oracle.combine_hidden_states(cw.aux[rows], cw.weight, cw.norm_weight, cw.eps,
+                                                               cw.dtype), cw.dtype)
+            hidden_bits = np.zeros_like(w.ctx_hidden)
+            hidden_bits[rows] = synthetic.to_bits(hid.astype(np.float32), w.dtype)
+            oracle.run_workload(dataclasses.replace(w, ctx_hidden=hidden_bits), sample=rows)
+            reps += 1
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": len(rows) * reps / el, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                               "sample": f"{len(rows)} tokens (combine then the write) x {reps} runs, {el:.1f} s, "
+                                         f"numpy float64"}
+    f.free()
+    return res
+
+
 COMBINE_METRIC = "combine_hidden_states tokens/s (main_proj GEMM + main_norm)"
 
 
@@ -941,7 +1089,8 @@ def main(argv=None):
                     help="kernel of the write (dspark_set_kernel_variant); auto picks by token count")
     ap.add_argument("--trace", action="store_true",
                     help="print per-CTA timelines of --steps traced writes instead of a bench line")
-    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify", "attention", "combine"],
+    ap.add_argument("--op", default="ctx_kv", choices=["ctx_kv", "qk_norm_rope", "verify", "attention", "combine",
+                                                   "fused"],
                     help="qk_norm_rope: the draft layers' in-place QK-norm + RoPE; verify: the "
                          "verify step's accepted-draft count and bonus token (instead of the write)")
     ap.add_argument("--source-hash", default=None, choices=sorted(KERNEL_SOURCES),
@@ -980,6 +1129,8 @@ def main(argv=None):
         out = run_attention(args)
     elif args.op == "combine":
         out = run_combine(args)
+    elif args.op == "fused":
+        out = run_fused(args)
     else:
         out = run_gpu(args, make(args))
     if out is not None:

@@ -24,6 +24,8 @@ __all__ = [
     "dspark_set_kernel_variant", "dspark_describe_schedule", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
     "dspark_correct_drafts_and_bonus", "dspark_draft_attention", "dspark_draft_attention_workspace_bytes",
     "Combine", "dspark_pack_combine", "dspark_combine_hidden_states", "dspark_combine_get_status",
+    "Fused", "dspark_pack_fused_ctx_kv", "dspark_combine_write_ctx_kv", "dspark_fused_get_status",
+    "dspark_fused_clear_status",
     "FLAG_POS_RANGE", "FLAG_LOC_RANGE", "FLAG_TIMEOUT",
 ]
 
@@ -486,6 +488,105 @@ def dspark_combine_get_status(c: Combine, stream=None) -> int:
     _abi.check(load().dspark_combine_get_status(c.handle, _stream_handle(stream), ctypes.byref(flags)),
                "dspark_combine_get_status")
     return flags.value
+
+
+class Fused:
+    """Handle of dspark_pack_fused_ctx_kv (combine_hidden_states fused into the
+    write); keeps the main_proj weight tensor alive, as the library does not
+    copy it."""
+
+    def __init__(self, handle, weight, hidden: int, aux_dim: int, dtype, num_layers: int, num_kv_heads: int,
+                 head_dim: int):
+        self.handle = handle
+        self.weight = weight
+        self.hidden = hidden
+        self.aux_dim = aux_dim
+        self.dtype = dtype
+        self.num_layers = num_layers
+        self.num_kv_heads = num_kv_heads
+        self.head_dim = head_dim
+
+    def free(self) -> None:
+        if self.handle:
+            load().dspark_free_fused(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def dspark_pack_fused_ctx_kv(main_proj_weight, main_norm_weight, norm_eps: float, layers: Sequence, stream=None) -> Fused:
+    """main_proj_weight [hidden, aux_dim] (the layers' dtype, unit column
+    stride), main_norm_weight [hidden]; layers as for dspark_pack_ctx_kv."""
+    w = main_proj_weight
+    if w.dim() != 2 or w.stride(1) != 1:
+        raise ValueError("main_proj_weight must be [hidden, aux_dim] with unit column stride")
+    if main_norm_weight.numel() != w.shape[0] or not main_norm_weight.is_contiguous():
+        raise ValueError("main_norm_weight must be a contiguous [hidden] tensor")
+    arr = _desc_array(layers)
+    out = ctypes.c_void_p()
+    code = load().dspark_pack_fused_ctx_kv(w.data_ptr(), w.shape[1], w.stride(0), main_norm_weight.data_ptr(),
+                                           _dtype_code(main_norm_weight.dtype), norm_eps, arr, len(layers),
+                                           w.shape[0], _stream_handle(stream), ctypes.byref(out))
+    _abi.check(code, "dspark_pack_fused_ctx_kv")
+    l0 = layers[0]
+    return Fused(out.value, w, w.shape[0], w.shape[1], w.dtype, len(layers), l0.num_kv_heads, l0.head_dim)
+
+
+def dspark_combine_write_ctx_kv(f: Fused, aux, positions, cos_sin, cache_loc, k_pools, v_pools,
+                                commit_lens=None, loc_row_width: Optional[int] = None, stream=None) -> None:
+    """The write with ctx_hidden = main_norm(main_proj(aux)) in one launch:
+    aux [T, aux_dim] in the handle's dtype (unit column stride); the other
+    arguments as for dspark_write_ctx_kv (pools as lists)."""
+    import torch
+    T = aux.shape[0]
+    if aux.dim() != 2 or aux.shape[1] != f.aux_dim or (T > 0 and aux.stride(1) != 1):
+        raise ValueError("aux must be [T, aux_dim] with unit column stride")
+    if aux.dtype != f.dtype:
+        raise TypeError("aux must be in the handle's dtype")
+    for name, t, dt in (("positions", positions, torch.int64), ("cache_loc", cache_loc, torch.int64),
+                        ("cos_sin", cos_sin, torch.float32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous {dt} tensor")
+    if commit_lens is not None and (commit_lens.dtype != torch.int32 or not commit_lens.is_contiguous()):
+        raise TypeError("commit_lens must be a contiguous int32 tensor")
+    if positions.numel() != T or cache_loc.numel() != T:
+        raise ValueError("positions and cache_loc must hold one entry per token")
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != f.head_dim:
+        raise ValueError(f"cos_sin must be [max_pos, head_dim={f.head_dim}]")
+    if len(k_pools) != f.num_layers or len(v_pools) != f.num_layers:
+        raise ValueError("one K and one V pool per layer")
+    slots = k_pools[0].shape[0]
+    for p in list(k_pools) + list(v_pools):
+        if (p.dim() != 3 or p.shape[0] != slots or p.shape[1] != f.num_kv_heads or p.shape[2] != f.head_dim
+                or p.stride(1) != f.head_dim or p.stride(2) != 1 or p.dtype != f.dtype):
+            raise ValueError("pools must be [slots, num_kv_heads, head_dim] in the handle's dtype with strides "
+                             "(*, head_dim, 1)")
+    L = f.num_layers
+    kstr = (ctypes.c_int64 * L)(*[p.stride(0) for p in k_pools])
+    vstr = (ctypes.c_int64 * L)(*[p.stride(0) for p in v_pools])
+    width = 0 if loc_row_width is None else int(loc_row_width)
+    nwin = 0 if commit_lens is None else commit_lens.numel()
+    code = load().dspark_combine_write_ctx_kv(
+        f.handle, aux.data_ptr(), T, aux.stride(0) if T > 0 else f.aux_dim, positions.data_ptr(),
+        cos_sin.data_ptr(), cos_sin.shape[0], cache_loc.data_ptr(),
+        None if commit_lens is None else commit_lens.data_ptr(), width, nwin, _ptr_array(k_pools),
+        _ptr_array(v_pools), kstr, vstr, _dtype_code(f.dtype), slots, _stream_handle(stream))
+    _abi.check(code, "dspark_combine_write_ctx_kv")
+
+
+def dspark_fused_get_status(f: Fused, stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    _abi.check(load().dspark_fused_get_status(f.handle, _stream_handle(stream), ctypes.byref(flags)),
+               "dspark_fused_get_status")
+    return flags.value
+
+
+def dspark_fused_clear_status(f: Fused, stream=None) -> None:
+    _abi.check(load().dspark_fused_clear_status(f.handle, _stream_handle(stream)), "dspark_fused_clear_status")
 
 
 def dspark_describe_schedule(tiles: int, num_kb: int, workers: int, split_first_allowed: bool = True) -> dict:

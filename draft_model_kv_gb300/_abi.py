@@ -135,6 +135,19 @@ def load() -> ctypes.CDLL:
     lib.dspark_combine_get_status.restype = ctypes.c_int
     lib.dspark_free_combine.argtypes = [vp]
     lib.dspark_free_combine.restype = None
+    lib.dspark_pack_fused_ctx_kv.argtypes = [vp, i64, i64, vp, i32, ctypes.c_float, ctypes.POINTER(LayerDesc), i32,
+                                             i32, vp, ctypes.POINTER(vp)]
+    lib.dspark_pack_fused_ctx_kv.restype = ctypes.c_int
+    lib.dspark_combine_write_ctx_kv.argtypes = [
+        vp, vp, i64, i64, vp, vp, i64, vp, vp, i64, i64,
+        ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64), ctypes.POINTER(i64), i32, i64, vp]
+    lib.dspark_combine_write_ctx_kv.restype = ctypes.c_int
+    lib.dspark_fused_get_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.dspark_fused_get_status.restype = ctypes.c_int
+    lib.dspark_fused_clear_status.argtypes = [vp, vp]
+    lib.dspark_fused_clear_status.restype = ctypes.c_int
+    lib.dspark_free_fused.argtypes = [vp]
+    lib.dspark_free_fused.restype = None
     lib.dspark_status_string.argtypes = [ctypes.c_int]
     lib.dspark_status_string.restype = ctypes.c_char_p
     _lib = lib

@@ -77,32 +77,79 @@ bool make_operand_map(CUtensorMap* map, const void* base, int dtype, uint64_t co
 
 using namespace dspark;
 
-struct dspark_bundle {
-  int device;
-  int dtype;
-  int L, H, NH, D, KV;
-  int64_t N;
-  int64_t w_pitch;      // elements between rows of w_all
-  void* w_all;          // [N, w_pitch] in dtype
-  void* bias;           // [N] in dtype or null
-  float* knorm;         // [L, D] fp32
-  uint32_t* status;     // device status word
-  float* workspace;     // partial tiles of the stream-K split (workspace_bytes(sms))
-  int32_t* counters;    // [sms] arrival counters, zero between launches
-  int sms;              // SM count of the bundle's device
-  uint64_t* trace;      // optional timeline buffer (dspark_set_trace_buffer)
-  int variant;          // DSPARK_VARIANT_* (dspark_set_kernel_variant)
-  int split_wait_extra;        // dspark_set_split_wait_test: arrivals no worker will make
-  uint64_t split_wait_ns;      // bound on the waits for a cut tile's published parts
-  CUtensorMap tmap_w_half;   // W_all with 128-row boxes (CTA-pair kernel)
-  float eps;
-  CUtensorMap tmap_w;
-};
+
 
 cudaError_t dspark::launch_to_fp32(const void* src, int dtype, float* dst, int n,
                                    cudaStream_t stream) {
   to_fp32_kernel<<<(n + 127) / 128, 128, 0, stream>>>(src, dtype, dst, n);
   return cudaGetLastError();
+}
+
+int dspark::fill_write_params(const dspark_bundle* b, const void* ctx_hidden, int64_t T,
+                              int64_t hidden_row_stride, int32_t hidden_dtype, const int64_t* positions,
+                              const float* cos_sin, int64_t max_pos, const int64_t* cache_loc,
+                              const int32_t* commit_lens, int64_t loc_row_width, int64_t num_windows,
+                              void* const* k_pools, void* const* v_pools, const int64_t* k_row_strides,
+                              const int64_t* v_row_strides, int32_t pool_dtype, int64_t pool_slots,
+                              WriteParams& p) {
+  if (b == nullptr) return DSPARK_E_INVALID_ARG;
+  if (T < 0) return DSPARK_E_INVALID_ARG;
+  if ((commit_lens != nullptr) != (loc_row_width != 0)) return DSPARK_E_COMMIT_ARGS;
+  if (commit_lens != nullptr) {
+    if (loc_row_width < 0 || num_windows < 0) return DSPARK_E_INVALID_ARG;
+    if (num_windows * loc_row_width != T) return DSPARK_E_NUMEL;
+  }
+  if (hidden_dtype != b->dtype || pool_dtype != b->dtype) return DSPARK_E_DTYPE_MISMATCH;
+  if (ctx_hidden == nullptr || positions == nullptr || cos_sin == nullptr || cache_loc == nullptr ||
+      k_pools == nullptr || v_pools == nullptr || k_row_strides == nullptr ||
+      v_row_strides == nullptr)
+    return DSPARK_E_INVALID_ARG;
+  if (max_pos <= 0 || pool_slots <= 0 || hidden_row_stride < b->H || T > 0x7FFFFFFFLL)
+    return DSPARK_E_INVALID_ARG;
+  if (!aligned16(ctx_hidden) || (hidden_row_stride * 2) % 16 != 0 || !aligned16(cos_sin))
+    return DSPARK_E_ALIGNMENT;
+  for (int l = 0; l < b->L; ++l) {
+    if (k_pools[l] == nullptr || v_pools[l] == nullptr) return DSPARK_E_INVALID_ARG;
+    if (k_row_strides[l] < b->KV || v_row_strides[l] < b->KV) return DSPARK_E_POOL_LAYOUT;
+    if (!aligned16(k_pools[l]) || !aligned16(v_pools[l]) || k_row_strides[l] % 8 != 0 ||
+        v_row_strides[l] % 8 != 0)
+      return DSPARK_E_ALIGNMENT;
+  }
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device != b->device) return DSPARK_E_DEVICE;
+  std::memset(&p, 0, sizeof(p));
+  p.T = static_cast<int32_t>(T);
+  p.H = b->H;
+  p.N = static_cast<int32_t>(b->N);
+  p.L = b->L;
+  p.NH = b->NH;
+  p.D = b->D;
+  p.KV = b->KV;
+  p.num_kb = (b->H + kTileK - 1) / kTileK;
+  p.positions = positions;
+  p.cache_loc = cache_loc;
+  p.commit_lens = commit_lens;
+  p.loc_row_width = commit_lens != nullptr ? loc_row_width : 0;
+  p.cos_sin = cos_sin;
+  p.max_pos = max_pos;
+  p.pool_slots = pool_slots;
+  p.knorm = b->knorm;
+  p.bias = b->bias;
+  p.eps = b->eps;
+  p.status = b->status;
+  p.workspace = b->workspace;
+  p.counters = b->counters;
+  p.trace = b->trace;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.split_wait_ns = b->split_wait_ns;
+  p.split_wait_extra = b->split_wait_extra;
+  for (int l = 0; l < b->L; ++l) {
+    p.k_pool[l] = k_pools[l];
+    p.v_pool[l] = v_pools[l];
+    p.k_stride[l] = k_row_strides[l];
+    p.v_stride[l] = v_row_strides[l];
+  }
+  return DSPARK_OK;
 }
 
 extern "C" {
@@ -245,66 +292,14 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
                         const int64_t* v_row_strides, int32_t pool_dtype, int64_t pool_slots,
                         void* stream_) {
   if (b == nullptr) return DSPARK_E_INVALID_ARG;
-  if (T < 0) return DSPARK_E_INVALID_ARG;
   if (T == 0) return DSPARK_OK;
-  if ((commit_lens != nullptr) != (loc_row_width != 0)) return DSPARK_E_COMMIT_ARGS;
-  if (commit_lens != nullptr) {
-    if (loc_row_width < 0 || num_windows < 0) return DSPARK_E_INVALID_ARG;
-    if (num_windows * loc_row_width != T) return DSPARK_E_NUMEL;
-  }
-  if (hidden_dtype != b->dtype || pool_dtype != b->dtype) return DSPARK_E_DTYPE_MISMATCH;
-  if (ctx_hidden == nullptr || positions == nullptr || cos_sin == nullptr || cache_loc == nullptr ||
-      k_pools == nullptr || v_pools == nullptr || k_row_strides == nullptr ||
-      v_row_strides == nullptr)
-    return DSPARK_E_INVALID_ARG;
-  if (max_pos <= 0 || pool_slots <= 0 || hidden_row_stride < b->H || T > 0x7FFFFFFFLL)
-    return DSPARK_E_INVALID_ARG;
-  if (!aligned16(ctx_hidden) || (hidden_row_stride * 2) % 16 != 0 || !aligned16(cos_sin))
-    return DSPARK_E_ALIGNMENT;
-  for (int l = 0; l < b->L; ++l) {
-    if (k_pools[l] == nullptr || v_pools[l] == nullptr) return DSPARK_E_INVALID_ARG;
-    if (k_row_strides[l] < b->KV || v_row_strides[l] < b->KV) return DSPARK_E_POOL_LAYOUT;
-    if (!aligned16(k_pools[l]) || !aligned16(v_pools[l]) || k_row_strides[l] % 8 != 0 ||
-        v_row_strides[l] % 8 != 0)
-      return DSPARK_E_ALIGNMENT;
-  }
-  int device = -1;
-  if (cudaGetDevice(&device) != cudaSuccess || device != b->device) return DSPARK_E_DEVICE;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-
   WriteParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.T = static_cast<int32_t>(T);
-  p.H = b->H;
-  p.N = static_cast<int32_t>(b->N);
-  p.L = b->L;
-  p.NH = b->NH;
-  p.D = b->D;
-  p.KV = b->KV;
-  p.num_kb = (b->H + kTileK - 1) / kTileK;
-  p.positions = positions;
-  p.cache_loc = cache_loc;
-  p.commit_lens = commit_lens;
-  p.loc_row_width = commit_lens != nullptr ? loc_row_width : 0;
-  p.cos_sin = cos_sin;
-  p.max_pos = max_pos;
-  p.pool_slots = pool_slots;
-  p.knorm = b->knorm;
-  p.bias = b->bias;
-  p.eps = b->eps;
-  p.status = b->status;
-  p.workspace = b->workspace;
-  p.counters = b->counters;
-  p.trace = b->trace;
-  p.wait_limit_ns = kWaitLimitNs;
-  p.split_wait_ns = b->split_wait_ns;
-  p.split_wait_extra = b->split_wait_extra;
-  for (int l = 0; l < b->L; ++l) {
-    p.k_pool[l] = k_pools[l];
-    p.v_pool[l] = v_pools[l];
-    p.k_stride[l] = k_row_strides[l];
-    p.v_stride[l] = v_row_strides[l];
-  }
+  const int st = fill_write_params(b, ctx_hidden, T, hidden_row_stride, hidden_dtype, positions, cos_sin, max_pos,
+                                   cache_loc, commit_lens, loc_row_width, num_windows, k_pools, v_pools,
+                                   k_row_strides, v_row_strides, pool_dtype, pool_slots, p);
+  if (st != DSPARK_OK) return st;
+  const int device = b->device;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
 
   // Small token counts: stream the weights (weights as the MMA's M side).
   int t_pad = 0, stages = 0;

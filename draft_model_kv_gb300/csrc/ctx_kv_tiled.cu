@@ -138,6 +138,35 @@ __device__ __forceinline__ void abort_work(const WriteParams& p, volatile int* a
 // was issued before the abort, and a tile load lands within microseconds.
 constexpr uint64_t kPairAbortDrainNs = 200000;
 
+// 1/rms over the first problem's columns of token row t (fused write): the
+// row's sums of squares per 256-column tile, added in a fixed order.
+__device__ __forceinline__ float row_inv_rms(const WriteParams& p, int64_t t) {
+  if (t >= p.T) return 0.f;
+  const float* r = p.rowsq + t * p.rowsq_stride;
+  float ss = 0.f;
+  for (int j = 0; j < p.rowsq_n; ++j) ss += r[j];
+  return 1.0f / sqrtf(ss / static_cast<float>(p.norm_n) + p.norm_eps);
+}
+
+// Generic-proxy stores to global memory before later tensor-memory (TMA)
+// loads of them, by this or another SM (with a release / acquire between).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Fused launch: wait (bounded) until every CTA is done with the first
+// problem, then order the loads that follow after it.
+__device__ __forceinline__ bool wait_first_problem(const WriteParams& p, volatile int* abort_flag) {
+  const int target = static_cast<int>(gridDim.x);
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_gpu(p.phase_count) < target) {
+    if (*abort_flag != 0 || global_timer_ns() - t0 > p.wait_limit_ns) return false;
+    __nanosleep(128);
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
 // The cut tiles of the split-first schedule (the tiles left over after the
 // full wave, whose k-blocks are spread over the workers).  Every contributor
 // publishes its part before any is read; then contributor i of n finishes
@@ -154,7 +183,7 @@ constexpr uint64_t kPairAbortDrainNs = 200000;
 // add their parts of the sum of squares through shared memory.  It runs on the
 // epilogue warps while the CTA's whole tile is on the tensor cores.  Returns
 // false if a wait ran out.
-template <typename E, int D, bool kBias, bool kPair>
+template <typename E, int D, bool kBias, bool kPair, bool kRowScale>
 __device__ bool finish_split_rows(const WriteParams& p, int wid, int nw, uint32_t rank, float* ss_part,
                                   volatile int* abort_flag) {
   using G = Geo<kPair>;
@@ -261,6 +290,14 @@ __device__ bool finish_split_rows(const WriteParams& p, int wid, int nw, uint32_
         const bool is_v = r >= p.KV;
         const int head = (is_v ? r - p.KV : r) / D;
         float x1[4] = {s1.x, s1.y, s1.z, s1.w}, x2[4] = {s2.x, s2.y, s2.z, s2.w};
+        if (kRowScale) {
+          const float rs = row_inv_rms(p, t);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x1[e] *= rs;
+            x2[e] *= rs;
+          }
+        }
         if (kBias && col_ok) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -310,11 +347,15 @@ __device__ bool finish_split_rows(const WriteParams& p, int wid, int nw, uint32_
   return true;
 }
 
-template <typename E, int D, bool kBias, bool kPair>
-__global__ void __launch_bounds__(kTiledThreads, 1)
-    ctx_kv_tiled_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                        const __grid_constant__ CUtensorMap tmap_w,
-                        const __grid_constant__ WriteParams p) {
+// The kernel body.  One problem (p with its operand maps), or with kFused two
+// in sequence in one launch: first p1 (the plain product main_proj, whose
+// output y is p's token operand), then p, each walking its own schedule over
+// the same pipeline; a grid-wide count of CTAs done with p1 orders p1's
+// stores before p's loads of them.
+template <typename E, int D, bool kBias, bool kPair, bool kFused>
+__device__ __forceinline__ void tiled_body(const CUtensorMap& tmap_x1, const CUtensorMap& tmap_w1,
+                                           const WriteParams& p1, const CUtensorMap& tmap_x,
+                                           const CUtensorMap& tmap_w, const WriteParams& p) {
   using G = Geo<kPair>;
   constexpr int kStages = G::kStages;
   constexpr uint32_t kStageBytesA = G::kStageA;
@@ -356,6 +397,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_w);
+    if (kFused) {
+      tma_prefetch_desc(&tmap_x1);
+      tma_prefetch_desc(&tmap_w1);
+    }
   }
   if (warp == kMmaWarp) {
     if (kPair) {
@@ -390,24 +435,36 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         // 45.2 -> 42.3 us.  With more token blocks the weights are kept
         // (evict_last) for the later groups.  The token rows are read by every
         // column block of their group: evict_last.
-        const uint64_t pol_w = p.num_m <= kGroupM ? l2_policy_evict_first() : l2_policy_evict_last();
-        const uint64_t pol_x = l2_policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
         uint32_t uses[kStages] = {};
         bool ok = true;
-        WorkIter it = work_begin(p, wid, nw);
+        for (int ph = kFused ? 0 : 1; ph < 2 && ok; ++ph) {
+        const WriteParams& wp = ph == 0 ? p1 : p;
+        const CUtensorMap* tx = ph == 0 ? &tmap_x1 : &tmap_x;
+        const CUtensorMap* tw = ph == 0 ? &tmap_w1 : &tmap_w;
+        const int nwq = kFused ? wp.workers : nw;
+        if (kFused && wid >= nwq) continue;
+        // the fused second problem reads the first one's output: every CTA
+        // must be done with the first one
+        if (kFused && ph == 1 && !wait_first_problem(p, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint64_t pol_w = wp.num_m <= kGroupM ? l2_policy_evict_first() : l2_policy_evict_last();
+        const uint64_t pol_x = l2_policy_evict_last();
+        WorkIter it = work_begin(wp, wid, nwq);
         int tile, kb0, kb1;
-        while (ok && work_next(p, it, tile, kb0, kb1)) {
+        while (ok && work_next(wp, it, tile, kb0, kb1)) {
           int m_blk, n_blk;
-          tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+          tile_coords(tile, wp.num_m, wp.num_n, m_blk, n_blk);
           const int a_row = m_blk * G::kTileRows + static_cast<int>(rank) * kTileM;
           const int b_row = n_blk * kTileN + static_cast<int>(rank) * G::kBRows;
           for (int kb = kb0; kb < kb1; ++kb) {
             const bool got = kPair ? mbar_wait_cluster(smem_u32(&bars->empty[stage]), phase ^ 1u,
-                                                       abort_flag, p.wait_limit_ns)
+                                                       abort_flag, wp.wait_limit_ns)
                                    : mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u,
-                                               abort_flag, p.wait_limit_ns);
+                                               abort_flag, wp.wait_limit_ns);
             if (!got) {
               ok = false;
               break;
@@ -417,15 +474,15 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
               // both CTAs' bytes complete on the leader's barrier
               if (leader) mbar_arrive_expect_tx(full, 2 * (kStageBytesA + kStageBytesB));
               const uint32_t full_leader = mapa_shared(full, 0);
-              tma_load_2d_pair(smem_u32(smem_a + stage * kStageBytesA), &tmap_x, kb * kTileK, a_row,
+              tma_load_2d_pair(smem_u32(smem_a + stage * kStageBytesA), tx, kb * kTileK, a_row,
                                full_leader, pol_x);
-              tma_load_2d_pair(smem_u32(smem_b + stage * kStageBytesB), &tmap_w, kb * kTileK, b_row,
+              tma_load_2d_pair(smem_u32(smem_b + stage * kStageBytesB), tw, kb * kTileK, b_row,
                                full_leader, pol_w);
             } else {
               mbar_arrive_expect_tx(full, kStageBytesA + kStageBytesB);
-              tma_load_2d(smem_u32(smem_a + stage * kStageBytesA), &tmap_x, kb * kTileK, a_row, full,
+              tma_load_2d(smem_u32(smem_a + stage * kStageBytesA), tx, kb * kTileK, a_row, full,
                           pol_x);
-              tma_load_2d(smem_u32(smem_b + stage * kStageBytesB), &tmap_w, kb * kTileK, b_row, full,
+              tma_load_2d(smem_u32(smem_b + stage * kStageBytesB), tw, kb * kTileK, b_row, full,
                           pol_w);
             }
             ++uses[stage];
@@ -434,6 +491,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
               phase ^= 1u;
             }
           }
+        }
         }
         if (!ok) abort_work<kPair>(p, abort_flag);
         // every load issued must land before the CTA may exit (bounded by time
@@ -465,18 +523,22 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         uint32_t acc_phase = 0;
         bool ok = true;
         bool issued = false;
-        WorkIter it = work_begin(p, wid, nw);
+        for (int ph = kFused ? 0 : 1; ph < 2 && ok; ++ph) {
+        const WriteParams& wp = ph == 0 ? p1 : p;
+        const int nwq = kFused ? wp.workers : nw;
+        if (kFused && wid >= nwq) continue;
+        WorkIter it = work_begin(wp, wid, nwq);
         int tile, kb0, kb1;
-        while (ok && work_next(p, it, tile, kb0, kb1)) {
+        while (ok && work_next(wp, it, tile, kb0, kb1)) {
           if (!mbar_wait_cluster(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort_flag,
-                                 p.wait_limit_ns)) {
+                                 wp.wait_limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kAccCols;
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait_cluster(smem_u32(&bars->full[stage]), phase, abort_flag, p.wait_limit_ns)) {
+            if (!mbar_wait_cluster(smem_u32(&bars->full[stage]), phase, abort_flag, wp.wait_limit_ns)) {
               ok = false;
               break;
             }
@@ -513,6 +575,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             acc_phase ^= 1u;
           }
         }
+        }
         if (!ok) abort_work<kPair>(p, abort_flag);
         if (issued) {
           // all MMAs issued by this thread complete before TMEM is released
@@ -531,8 +594,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     // D == 0: plain product mode (main_proj of combine_hidden_states): the
     // tile is stored in the model dtype with per-row sums of squares of the
     // stored values; no tokens, pools or heads are involved
-    constexpr bool kPlain = D == 0;
     constexpr int kHalf = D / 2;
+    // head width of the write's code paths (never run with D == 0: the plain
+    // mode takes its own branch)
+    constexpr int kD = D == 0 ? 128 : D;
     // cos/sin staging for the last item: measured to pay off for D = 128 only
     constexpr bool kStageCs = D == 128;
     constexpr uint32_t kCsBytes = kStageCs ? kTileM * D * 4 : 0;
@@ -548,29 +613,46 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     uint32_t acc_phase = 0;
     uint32_t fix_phase = 0;   // parity of this group's fix barrier
     int item = 0;
-    WorkIter it = work_begin(p, wid, nw);
+    bool ep_abort = false;
+    for (int ph = kFused ? 0 : 1; ph < 2 && !ep_abort; ++ph) {
+    const WriteParams& wp = ph == 0 ? p1 : p;
+    const int nwq = kFused ? wp.workers : nw;
+    // D == 0, or the first problem of a fused launch: plain product mode
+    const bool plain = D == 0 || (kFused && ph == 0);
+    if (kFused && ph == 1) {
+      // the row scales of the second problem are the first one's row sums
+      const bool got = wait_first_problem(p, abort_flag);
+      if (!named_barrier_and(1, kEpiThreads, got)) {
+        if (etid == 0) abort_work<kPair>(p, abort_flag);
+        break;
+      }
+    }
+    WorkIter it = work_begin(wp, wid, kFused && wid >= nwq ? 1 : nwq);
+    if (kFused && wid >= nwq) it.dp_tile = wp.dp_tiles, it.cur = it.start = 0;   // no work in this problem
     int tile, kb0, kb1;
-    while (work_next(p, it, tile, kb0, kb1)) {
+    while (work_next(wp, it, tile, kb0, kb1)) {
       int m_blk, n_blk;
-      tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+      tile_coords(tile, wp.num_m, wp.num_n, m_blk, n_blk);
       // split-first schedule: after the last part of the stream-K range is
       // published, finish this worker's share of its cut tiles
-      const bool reduce_after = p.sk_first && tile >= p.dp_tiles && it.cur <= it.start;
+      const bool reduce_after = wp.sk_first && tile >= wp.dp_tiles && it.cur <= it.start;
       bool final_item;
       {
         WorkIter peek = it;
         int t2, a2, b2;
-        final_item = !work_next(p, peek, t2, a2, b2);
+        final_item = !work_next(wp, peek, t2, a2, b2);
       }
       // ---- per-token decision (same for every head of the tile); it does not
       // depend on the accumulator, so it runs while the MMAs are in flight
       const int64_t row0 = static_cast<int64_t>(m_blk) * G::kTileRows + static_cast<int64_t>(rank) * kTileM;
       const int64_t t = row0 + row;
       int64_t loc = 0, pos = 0;
-      const bool write = !kPlain && token_write(p, t, group == 0, loc, pos);
+      const bool write = !plain && token_write(wp, t, group == 0, loc, pos);
+      // fused second problem: this token row's 1/rms of y (main_norm)
+      const float rs = (kFused && !plain) ? row_inv_rms(wp, t) : 1.f;
       if (write) {
         // the K heads of this tile will read this token's cos/sin row
-        const char* cs_row = reinterpret_cast<const char*>(p.cos_sin + pos * D);
+        const char* cs_row = reinterpret_cast<const char*>(wp.cos_sin + pos * D);
         for (int b = group * 128; b < D * 4; b += 256) prefetch_l2(cs_row + b);
       }
       // A tile cut between workers (whole-tiles-first order) is finished by
@@ -581,22 +663,22 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // workers and every CTA is resident (at most one per SM), so they end.
       // The finisher looks now, while its MMAs run, whether the other parts
       // are already published (read after the barrier below).
-      const bool cut = kb0 != 0 || kb1 != p.num_kb;
+      const bool cut = kb0 != 0 || kb1 != wp.num_kb;
       int c_first = 0, c_last = 0;
       if (cut) {
-        const int64_t u0 = static_cast<int64_t>(tile - p.dp_tiles) * p.num_kb;
-        c_first = sk_owner(p, u0);
-        c_last = sk_owner(p, u0 + p.num_kb - 1);
+        const int64_t u0 = static_cast<int64_t>(tile - wp.dp_tiles) * wp.num_kb;
+        c_first = sk_owner(wp, u0);
+        c_last = sk_owner(wp, u0 + wp.num_kb - 1);
       }
       auto cta_of = [&](int c) { return kPair ? 2 * c + static_cast<int>(rank) : c; };
-      const bool designated = cut && !p.sk_first && wid == c_last;
+      const bool designated = cut && !wp.sk_first && wid == c_last;
       if (designated && etid == 0) {
-        const int seen = ld_acquire_gpu(p.counters + cta_of(c_last));
-        *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first + p.split_wait_extra;
+        const int seen = ld_acquire_gpu(wp.counters + cta_of(c_last));
+        *reinterpret_cast<volatile int*>(&bars->last_arrival) = seen == c_last - c_first + wp.split_wait_extra;
       }
       // the outcome must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = mbar_wait_cluster(smem_u32(&bars->tmem_full[acc]), acc_phase, abort_flag,
-                                         p.wait_limit_ns);
+                                         wp.wait_limit_ns);
       // stamps come from the thread of row 0 of the first group
       uint64_t* tr =
           (trace != nullptr && etid == 0 && item < kTraceItems) ? trace + 3 + 6 * item : nullptr;
@@ -610,7 +692,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // every epilogue warp takes the same decision (they meet at named
       // barriers below), and every wait ends within its time bound
       if (!named_barrier_and(1, kEpiThreads, got)) {
-        if (etid == 0) abort_work<kPair>(p, abort_flag);
+        if (etid == 0) abort_work<kPair>(wp, abort_flag);
+        ep_abort = true;
         break;
       }
       tc_fence_after();
@@ -622,16 +705,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // that the row-per-thread reads below are free of bank conflicts): the
       // rotation then reads shared memory instead of waiting on L2 per chunk.
       bool tile_has_k = false;
-      if constexpr (!kPlain) {
-        for (int seg = 0; seg < kTileN / D; ++seg) {
-          const int c0 = n_blk * kTileN + seg * D;
-          if (c0 < p.N && c0 % (2 * p.KV) < p.KV) tile_has_k = true;
+      if (!plain) {
+        for (int seg = 0; seg < kTileN / kD; ++seg) {
+          const int c0 = n_blk * kTileN + seg * kD;
+          if (c0 < wp.N && c0 % (2 * wp.KV) < wp.KV) tile_has_k = true;
         }
       }
       const bool cs_stage = kStageCs && final_item && tile_has_k;
       auto stage_cs = [&]() {
         if (!cs_stage || !write) return;
-        const char* src = reinterpret_cast<const char*>(p.cos_sin + pos * D);
+        const char* src = reinterpret_cast<const char*>(wp.cos_sin + pos * D);
         const uint32_t dst = smem_u32(smem) + static_cast<uint32_t>(row) * (D * 4);
         constexpr int kUnits = D / 4;   // 16-byte units per row
 #pragma unroll
@@ -643,25 +726,26 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // finisher) wait for the other parts and add them in contributor order
       bool finish = true;
       if (cut) {
-        int32_t* counter = p.counters + cta_of(c_last);
+        int32_t* counter = wp.counters + cta_of(c_last);
         finish = designated;
         if (designated) {
           const bool early = *reinterpret_cast<volatile int*>(&bars->last_arrival) != 0;
           bool ok = true;
           if (!early && etid == 0)
-            ok = wait_count(counter, c_last - c_first + p.split_wait_extra, abort_flag, p.split_wait_ns);
+            ok = wait_count(counter, c_last - c_first + wp.split_wait_extra, abort_flag, wp.split_wait_ns);
           if (!named_barrier_and(1, kEpiThreads, ok)) {
-            if (etid == 0) abort_work<kPair>(p, abort_flag);
+            if (etid == 0) abort_work<kPair>(wp, abort_flag);
+            ep_abort = true;
             break;
           }
           if (etid == 0) *counter = 0;   // no other contributor touches it again
         } else {
-          float4* mine = reinterpret_cast<float4*>(ws_slot(p, cta_of(wid), kb0 > 0 ? 0 : 1));
+          float4* mine = reinterpret_cast<float4*>(ws_slot(wp, cta_of(wid), kb0 > 0 ? 0 : 1));
 #pragma unroll 1
           for (int ch = ch_lo; ch < ch_hi; ch += 2) {
             uint32_t v[32], u[32];
             tmem_ld32x2(t_row + ch * 32, t_row + (ch + 1) * 32, v, u);
-            if (t < p.T) {
+            if (t < wp.T) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 __stcg(mine + (ch * 8 + j) * kTileM + row,
@@ -686,7 +770,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           // accumulator = sum of all parts in ascending contributor order (this
           // CTA's own part taken from TMEM at its place), so the bits do not
           // depend on timing.  Each group sums its half of the columns.
-          const int64_t rows_left = static_cast<int64_t>(p.T) - row0;
+          const int64_t rows_left = static_cast<int64_t>(wp.T) - row0;
           const int rv = rows_left <= 0 ? 0 : (rows_left < kTileM ? static_cast<int>(rows_left) : kTileM);
           const int n_oth = c_last - c_first;
           // The operand ring is idle after the CTA's last MMA: the other parts
@@ -720,7 +804,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                 int oi = 0;
                 for (int c = c_first; c <= c_last; ++c) {
                   if (c == wid) continue;
-                  const float* slot = ws_slot(p, cta_of(c), c == c_first ? 1 : 0);
+                  const float* slot = ws_slot(wp, cta_of(c), c == c_first ? 1 : 0);
                   for (int cl = 0; cl < nch; ++cl)
                     bulk_load_g2s(ring + static_cast<uint32_t>(oi * nch + cl) * kChunkBytes,
                                   slot + static_cast<size_t>(ch0 + cl) * 8 * kTileM * 4, kChunkBytes, fbar);
@@ -731,7 +815,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
               // copies read valid workspace and always complete: the wait
               // does not stop on an abort, so none is left in flight)
               int never = 0;
-              fix_ok = mbar_wait(fbar, fix_phase, &never, p.wait_limit_ns) && fix_ok;
+              fix_ok = mbar_wait(fbar, fix_phase, &never, wp.wait_limit_ns) && fix_ok;
               fix_phase ^= 1u;
             }
 #pragma unroll 1
@@ -747,7 +831,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                   if (row < rv && fix_ok) {
                     const float4* src =
                         staged ? ring_f4 + (oi * nch + cl) * 8 * kTileM + row
-                               : reinterpret_cast<const float4*>(ws_slot(p, cta_of(c), c == c_first ? 1 : 0)) +
+                               : reinterpret_cast<const float4*>(ws_slot(wp, cta_of(c), c == c_first ? 1 : 0)) +
                                      ch * 8 * kTileM + row;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -773,7 +857,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             // the group's staging half is rewritten by its next round
             if (staged && n_oth > 0) named_barrier(2 + group, 128);
           }
-          if (!fix_ok && etid % 128 == 0) abort_work<kPair>(p, abort_flag);
+          if (!fix_ok && etid % 128 == 0) abort_work<kPair>(wp, abort_flag);
           // both groups' sums are in TMEM before any thread reads across halves
           tc_fence_before();
           named_barrier(1, kEpiThreads);
@@ -787,7 +871,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         named_barrier(1, kEpiThreads);   // both halves of every row have landed
       }
       if (tr != nullptr && finish) tr[4] = global_timer_ns();
-      if constexpr (kPlain) {
+      if (plain) {
         if (finish) {
           // this group's 128 columns of the row: stored rounded to the model
           // dtype; the sum of squares is taken over the stored values
@@ -797,13 +881,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           for (int ch = 0; ch < kChunks / 2; ch += 2) {
             uint32_t v[32], u[32];
             tmem_ld32x2(t_row + (ch_lo + ch) * 32, t_row + (ch_lo + ch + 1) * 32, v, u);
-            if (t < p.T) {
+            if (t < wp.T) {
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
                 const uint32_t* src = half == 0 ? v : u;
                 const int c = col0 + (ch + half) * 32;
-                if (c >= p.N) continue;
-                E* dst = reinterpret_cast<E*>(p.y) + t * p.y_stride + c;
+                if (c >= wp.N) continue;
+                E* dst = reinterpret_cast<E*>(wp.y) + t * wp.y_stride + c;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                   uint32_t w[4];
@@ -823,21 +907,21 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           // the two groups' halves of the row, added in a fixed order
           if (group == 1) bars->ss_x[row] = ss;
           named_barrier(1, kEpiThreads);
-          if (group == 0 && t < p.T) p.rowsq[t * p.rowsq_stride + n_blk] = ss + bars->ss_x[row];
+          if (group == 0 && t < wp.T) wp.rowsq[t * wp.rowsq_stride + n_blk] = ss + bars->ss_x[row];
           named_barrier(1, kEpiThreads);
         }
       } else if (finish) {
 #pragma unroll 1
-        for (int seg = group; seg < kTileN / D; seg += 2) {
-          const int c0 = n_blk * kTileN + seg * D;
-          if (c0 >= p.N) break;
-          const int layer = c0 / (2 * p.KV);
-          const int r = c0 - layer * 2 * p.KV;
-          const bool is_v = r >= p.KV;
-          const int head = (is_v ? r - p.KV : r) / D;
+        for (int seg = group; seg < kTileN / kD; seg += 2) {
+          const int c0 = n_blk * kTileN + seg * kD;
+          if (c0 >= wp.N) break;
+          const int layer = c0 / (2 * wp.KV);
+          const int r = c0 - layer * 2 * wp.KV;
+          const bool is_v = r >= wp.KV;
+          const int head = (is_v ? r - wp.KV : r) / kD;
           const uint32_t t_seg = t_row + seg * D;
           if (is_v) {
-            E* dst = reinterpret_cast<E*>(p.v_pool[layer]) + loc * p.v_stride[layer] + head * D;
+            E* dst = reinterpret_cast<E*>(wp.v_pool[layer]) + loc * wp.v_stride[layer] + head * D;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ch += 2) {
               uint32_t v[32], u[32];
@@ -848,13 +932,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                   float x[8], y[8];
 #pragma unroll
                   for (int e = 0; e < 8; ++e) {
-                    x[e] = f32(v[8 * q + e]);
-                    y[e] = f32(u[8 * q + e]);
+                    x[e] = f32(v[8 * q + e]) * rs;
+                    y[e] = f32(u[8 * q + e]) * rs;
                   }
                   if (kBias) {
                     float bx[8], by[8];
-                    load8<E>(p.bias, c0 + ch * 32 + 8 * q, bx);
-                    load8<E>(p.bias, c0 + (ch + 1) * 32 + 8 * q, by);
+                    load8<E>(wp.bias, c0 + ch * 32 + 8 * q, bx);
+                    load8<E>(wp.bias, c0 + (ch + 1) * 32 + 8 * q, by);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                       x[e] += bx[e];
@@ -881,12 +965,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
               for (int q = 0; q < 4; ++q) {
                 float bx[8], by[8];
                 if (kBias) {
-                  load8<E>(p.bias, c0 + ch * 32 + 8 * q, bx);
-                  load8<E>(p.bias, c0 + (ch + 1) * 32 + 8 * q, by);
+                  load8<E>(wp.bias, c0 + ch * 32 + 8 * q, bx);
+                  load8<E>(wp.bias, c0 + (ch + 1) * 32 + 8 * q, by);
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                  float x = f32(v[8 * q + e]), y = f32(u[8 * q + e]);
+                  float x = f32(v[8 * q + e]) * rs, y = f32(u[8 * q + e]) * rs;
                   if (kBias) {
                     x += bx[e];
                     y += by[e];
@@ -896,11 +980,11 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                 }
               }
             }
-            const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
-            const float* w = p.knorm + static_cast<int64_t>(layer) * D;
-            const float* cs = p.cos_sin + pos * D;
+            const float inv = rsqrtf(ss * (1.0f / D) + wp.eps);
+            const float* w = wp.knorm + static_cast<int64_t>(layer) * D;
+            const float* cs = wp.cos_sin + pos * D;
             const uint8_t* cs_smem = smem + static_cast<size_t>(row) * (D * 4);
-            E* dst = reinterpret_cast<E*>(p.k_pool[layer]) + loc * p.k_stride[layer] + head * D;
+            E* dst = reinterpret_cast<E*>(wp.k_pool[layer]) + loc * wp.k_stride[layer] + head * D;
             // rotate 16 columns of each half at a time (bounded register use)
 #pragma unroll 1
             for (int hc = 0; hc < kHalf / 16; ++hc) {
@@ -910,10 +994,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                 uint32_t o1[8], o2[8];
                 float b1[16], b2[16];
                 if (kBias) {
-                  load8<E>(p.bias, c0 + hc * 16, *reinterpret_cast<float(*)[8]>(&b1[0]));
-                  load8<E>(p.bias, c0 + hc * 16 + 8, *reinterpret_cast<float(*)[8]>(&b1[8]));
-                  load8<E>(p.bias, c0 + kHalf + hc * 16, *reinterpret_cast<float(*)[8]>(&b2[0]));
-                  load8<E>(p.bias, c0 + kHalf + hc * 16 + 8, *reinterpret_cast<float(*)[8]>(&b2[8]));
+                  load8<E>(wp.bias, c0 + hc * 16, *reinterpret_cast<float(*)[8]>(&b1[0]));
+                  load8<E>(wp.bias, c0 + hc * 16 + 8, *reinterpret_cast<float(*)[8]>(&b1[8]));
+                  load8<E>(wp.bias, c0 + kHalf + hc * 16, *reinterpret_cast<float(*)[8]>(&b2[0]));
+                  load8<E>(wp.bias, c0 + kHalf + hc * 16 + 8, *reinterpret_cast<float(*)[8]>(&b2[8]));
                 }
 #pragma unroll
                 for (int e4 = 0; e4 < 16; e4 += 4) {
@@ -936,8 +1020,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                   float r1[4], r2[4];
 #pragma unroll
                   for (int j = 0; j < 4; ++j) {
-                    float x1 = f32(a[e4 + j]);
-                    float x2 = f32(b[e4 + j]);
+                    float x1 = f32(a[e4 + j]) * rs;
+                    float x2 = f32(b[e4 + j]) * rs;
                     if (kBias) {
                       x1 += b1[e4 + j];
                       x2 += b2[e4 + j];
@@ -977,12 +1061,29 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         acc_phase ^= 1u;
       }
       if (reduce_after) {
-        if (!finish_split_rows<E, D, kBias, kPair>(p, wid, nw, rank, bars->ss_x, abort_flag)) {
-          if (etid == 0) abort_work<kPair>(p, abort_flag);
+        const bool split_ok =
+            plain ? finish_split_rows<E, 0, false, kPair, false>(wp, wid, nwq, rank, bars->ss_x, abort_flag)
+                  : finish_split_rows<E, D, kBias, kPair, kFused>(wp, wid, nwq, rank, bars->ss_x, abort_flag);
+        if (!split_ok) {
+          if (etid == 0) abort_work<kPair>(wp, abort_flag);
+          ep_abort = true;
           break;
         }
         if (trace != nullptr && etid == 0) trace[kTraceWords - 1] = global_timer_ns();   // split rows done
       }
+    }
+    if (kFused && ph == 0 && !ep_abort) {
+      // this CTA's part of the first problem (y and its row sums) is stored:
+      // make it visible to the tensor-memory loads of the second one and count
+      // the CTA done
+      fence_proxy_async_global();
+      named_barrier(1, kEpiThreads);
+      if (etid == 0) atom_add_acq_rel_gpu(p.phase_count, 1);
+    }
+    }
+    if (kFused && !ep_abort && etid == 0) {
+      // second round: the last CTA to finish resets the count for the next launch
+      if (atom_add_acq_rel_gpu(p.phase_count, 1) == 2 * static_cast<int>(gridDim.x) - 1) *p.phase_count = 0;
     }
   }
 
@@ -1007,6 +1108,28 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     while (work_next(p, it, tile, kb0, kb1)) ++n;
     trace[2] = static_cast<uint64_t>(n);
   }
+}
+
+template <typename E, int D, bool kBias, bool kPair>
+__global__ void __launch_bounds__(kTiledThreads, 1)
+    ctx_kv_tiled_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                        const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ WriteParams p) {
+  tiled_body<E, D, kBias, kPair, false>(tmap_x, tmap_w, p, tmap_x, tmap_w, p);
+}
+
+// combine_hidden_states fused into the write: main_proj (p1, plain mode, y and
+// its row sums into scratch) then the write (p) over y with the stacked
+// weights scaled by main_norm's weight and every token row by its 1/rms.
+template <typename E, int D, bool kBias>
+__global__ void __launch_bounds__(kTiledThreads, 1)
+    ctx_kv_fused_kernel(const __grid_constant__ CUtensorMap tmap_x1,
+                        const __grid_constant__ CUtensorMap tmap_w1,
+                        const __grid_constant__ WriteParams p1,
+                        const __grid_constant__ CUtensorMap tmap_x,
+                        const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ WriteParams p) {
+  tiled_body<E, D, kBias, true, true>(tmap_x1, tmap_w1, p1, tmap_x, tmap_w, p);
 }
 
 template <bool kPair>
@@ -1094,6 +1217,60 @@ cudaError_t launch_plain(int device, int dtype, const CUtensorMap& tx, const CUt
                          int grid, bool pair, cudaStream_t stream) {
   return pair ? dispatch_plain<true>(device, dtype, tx, tw, p, grid, stream)
               : dispatch_plain<false>(device, dtype, tx, tw, p, grid, stream);
+}
+
+namespace {
+
+template <typename E, int D, bool kBias>
+cudaError_t launch_fused_one(int device, const CUtensorMap& tx1, const CUtensorMap& tw1, const WriteParams& p1,
+                             const CUtensorMap& tx, const CUtensorMap& tw, const WriteParams& p, int grid,
+                             cudaStream_t stream) {
+  auto kern = ctx_kv_fused_kernel<E, D, kBias>;
+  static std::atomic<uint64_t> attr_set{0};
+  const uint64_t bit = 1ull << (device & 63);
+  const size_t smem = tiled_smem_bytes<true>();
+  if (!(attr_set.load() & bit)) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (static_cast<long>(fa.numRegs) * kTiledThreads < 128L * kRegsControl + 256L * kRegsEpilogue)
+      return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kTiledThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tx1, tw1, p1, tx, tw, p);
+}
+
+}  // namespace
+
+cudaError_t launch_fused(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tx1,
+                         const CUtensorMap& tw1, const WriteParams& p1, const CUtensorMap& tx,
+                         const CUtensorMap& tw_half, const WriteParams& p, int grid, cudaStream_t stream) {
+  if (dtype == DSPARK_DTYPE_BF16) {
+    if (head_dim == 128)
+      return has_bias ? launch_fused_one<__nv_bfloat16, 128, true>(device, tx1, tw1, p1, tx, tw_half, p, grid, stream)
+                      : launch_fused_one<__nv_bfloat16, 128, false>(device, tx1, tw1, p1, tx, tw_half, p, grid, stream);
+    return has_bias ? launch_fused_one<__nv_bfloat16, 64, true>(device, tx1, tw1, p1, tx, tw_half, p, grid, stream)
+                    : launch_fused_one<__nv_bfloat16, 64, false>(device, tx1, tw1, p1, tx, tw_half, p, grid, stream);
+  }
+  if (head_dim == 128)
+    return has_bias ? launch_fused_one<__half, 128, true>(device, tx1, tw1, p1, tx, tw_half, p, grid, stream)
+                    : launch_fused_one<__half, 128, false>(device, tx1, tw1, p1, tx, tw_half, p, grid, stream);
+  return has_bias ? launch_fused_one<__half, 64, true>(device, tx1, tw1, p1, tx, tw_half, p, grid, stream)
+                  : launch_fused_one<__half, 64, false>(device, tx1, tw1, p1, tx, tw_half, p, grid, stream);
 }
 
 cudaError_t launch_pair(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tx,

@@ -6,6 +6,8 @@
 
 #include "../../include/dspark_ctx_kv.h"
 
+struct dspark_bundle;
+
 namespace dspark {
 
 constexpr int kMaxDpPerm = 160;   // whole tiles that a launch may reorder (one wave of SMs)
@@ -48,6 +50,16 @@ struct WriteParams {
   // optional order of the whole tiles: worker w's i-th whole tile is
   // dp_perm[w + i*workers] when that index is below dp_perm_n (else itself)
   int32_t dp_perm_n;
+  // fused launch (combine_hidden_states then the write, ctx_kv_fused_kernel):
+  // this problem's worker count; the grid-wide count of CTAs done with the
+  // first problem (zero between launches); for the write, the first problem's
+  // row sums of squares (rowsq, rowsq_stride, rowsq_n tiles) give each token
+  // row's scale 1/sqrt(sum / norm_n + norm_eps)
+  int32_t workers;
+  int32_t* phase_count;
+  int32_t rowsq_n;
+  int32_t norm_n;
+  float norm_eps;
   uint64_t* trace;              // null, or [gridDim.x][kTraceWords] timeline stamps
   float* workspace;             // [gridDim.x][2][kTileN/4][kTileM][4] fp32 partial tiles
   int32_t* counters;            // [gridDim.x] arrivals per cut tile, reset by the last one
@@ -204,6 +216,15 @@ cudaError_t launch_stream(int device, int dtype, int head_dim, bool has_bias, co
 cudaError_t launch_plain(int device, int dtype, const CUtensorMap& tmap_x, const CUtensorMap& tmap_w,
                          const WriteParams& p, int grid, bool pair, cudaStream_t stream);
 
+// combine_hidden_states fused into the write, one launch of CTA pairs: p1 is
+// main_proj in plain mode (token operand tmap_x1 = aux, weights tmap_w1 =
+// main_proj with 128-row boxes; y and its row sums into p1.y / p1.rowsq), p
+// the write whose token operand tmap_x is y and whose stacked weights are
+// scaled by main_norm's weight.  grid = 2 x max(p1.workers, p.workers).
+cudaError_t launch_fused(int device, int dtype, int head_dim, bool has_bias, const CUtensorMap& tmap_x1,
+                         const CUtensorMap& tmap_w1, const WriteParams& p1, const CUtensorMap& tmap_x,
+                         const CUtensorMap& tmap_w_half, const WriteParams& p, int grid, cudaStream_t stream);
+
 // 2-D K-major operand map (api.cu): rows of `cols` 16-bit elements,
 // `pitch_elems` apart; boxes of kTileK x box_rows with the 128-byte swizzle;
 // out-of-range rows/columns read as zero.  False if the driver refuses it.
@@ -218,7 +239,41 @@ int pair_workers(int device);
 int single_workers(int device);
 int stream_workers(int device, int stages, uint32_t stage_b);
 
+// Validate the arguments of a write with bundle `b` and fill everything of p
+// but the work split (dims, inputs, pools, bundle buffers, bounds).  Returns a
+// dspark_status; nothing is enqueued.
+int fill_write_params(const dspark_bundle* b, const void* ctx_hidden, int64_t T, int64_t hidden_row_stride,
+                      int32_t hidden_dtype, const int64_t* positions, const float* cos_sin, int64_t max_pos,
+                      const int64_t* cache_loc, const int32_t* commit_lens, int64_t loc_row_width,
+                      int64_t num_windows, void* const* k_pools, void* const* v_pools,
+                      const int64_t* k_row_strides, const int64_t* v_row_strides, int32_t pool_dtype,
+                      int64_t pool_slots, WriteParams& p);
+
 // Convert a [n] bf16 / fp16 / fp32 vector to fp32 (bundle packing).
 cudaError_t launch_to_fp32(const void* src, int dtype, float* dst, int n, cudaStream_t stream);
 
 }  // namespace dspark
+
+// A packed bundle (dspark_pack_ctx_kv): the stacked K|V weights and their
+// tensor maps, fp32 k_norm weights, and the scratch every write with it uses.
+struct dspark_bundle {
+  int device;
+  int dtype;
+  int L, H, NH, D, KV;
+  int64_t N;
+  int64_t w_pitch;      // elements between rows of w_all
+  void* w_all;          // [N, w_pitch] in dtype
+  void* bias;           // [N] in dtype or null
+  float* knorm;         // [L, D] fp32
+  uint32_t* status;     // device status word
+  float* workspace;     // partial tiles of the stream-K split (workspace_bytes(sms))
+  int32_t* counters;    // [sms] arrival counters, zero between launches
+  int sms;              // SM count of the bundle's device
+  uint64_t* trace;      // optional timeline buffer (dspark_set_trace_buffer)
+  int variant;          // DSPARK_VARIANT_* (dspark_set_kernel_variant)
+  int split_wait_extra;        // dspark_set_split_wait_test: arrivals no worker will make
+  uint64_t split_wait_ns;      // bound on the waits for a cut tile's published parts
+  CUtensorMap tmap_w_half;   // W_all with 128-row boxes (CTA-pair kernel)
+  float eps;
+  CUtensorMap tmap_w;
+};
