@@ -371,7 +371,7 @@ KERNEL_SOURCES = {
     "ctx_kv": ["ctx_kv_tiled.cu", "ctx_kv_stream.cu", "kernel_common.cuh", "internal.h", "ptx.cuh",
                "api.cu"],
     "qk_norm_rope": ["qk_norm_rope.cu"],
-    "attention": ["draft_attention.cu"],
+    "attention": ["draft_attention.cu", "ptx.cuh"],
     "combine": ["ctx_kv_tiled.cu", "kernel_common.cuh", "internal.h", "ptx.cuh", "combine.cu"],
     "fused": ["ctx_kv_tiled.cu", "kernel_common.cuh", "internal.h", "ptx.cuh", "fused.cu", "api.cu"],
 }

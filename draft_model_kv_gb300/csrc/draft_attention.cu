@@ -10,25 +10,31 @@
 //   S^T[key][row]  = K_g[key] . Q_g[row]            M = 128 keys, N = rows, K = D
 //   O^T[d][row]   += V_g^T[d][key] . P^T[row][key]  M = 128 (d), N = rows, K = 128 keys
 //
-// both accumulated in TMEM (S double-buffered).  Four producer warps gather,
-// per 128-key chunk, each key's 2 x D x 2 bytes of head g (its K and V rows of
-// the pool, or of the block's own keys for the last chunk of split 0) with
-// 16-byte asynchronous copies into the 128-byte-swizzled layout of the MMA
-// operands, three stages deep; the staged chunk is the K-major A operand of
-// the first product and, read as an MN-major operand, the V^T of the second.
-// Four softmax warps own one key (TMEM lane) each: they load the key's scores
-// for every query row, take the per-row maximum and sum over the 128 keys with
-// warp transpose-reductions, run the online softmax in the log2 domain, write
-// P^T (model dtype) to shared memory as the B operand of the second product
-// and rescale O^T in TMEM when a row's maximum grows by more than 2^8 (so the
-// softmax seldom waits for the previous product).  One thread issues the
-// MMAs.  Each split writes its unnormalised O, maximum and sum to the
-// workspace; stage 2 merges the splits of each query row with the
-// log-sum-exp weights and stores the output in the model dtype.
+// both accumulated in TMEM (S double-buffered; O once per group of 32 keys).
+// Four producer warps gather, per 128-key chunk, each key's 2 x D x 2 bytes of
+// head g (its K and V rows of the pool, or of the block's own keys for the
+// last chunk of split 0) with 16-byte asynchronous copies into the
+// 128-byte-swizzled layout of the MMA operands, three stages deep, a warp
+// instruction covering a key's whole rows; the staged chunk is the K-major A
+// operand of the first product and, read as an MN-major operand, the V^T of
+// the second.  Eight softmax warps, two warpgroups of 16 query rows, own one
+// key (TMEM lane) per thread.  Each warp keeps its own running maximum and
+// sum per row over its 32 keys of every chunk (warp transpose-reductions, no
+// exchange with the other warps), writes P^T (model dtype) to shared memory as
+// the B operand of the second product, whose 32-key groups accumulate into
+// four separate O^T, and raises its maximum only when a chunk exceeds it by
+// more than 2^8; the warps of a warpgroup meet once per chunk to rescale the
+// O^T of the warps whose maximum grew.  The four partial results of a row are
+// merged when the split ends.  One thread issues the MMAs as their inputs
+// become ready: the scores of the next landed chunk, and the product of the
+// oldest chunk whose P^T is written.  Each split writes its unnormalised O,
+// maximum and sum to the workspace; stage 2 merges the splits of each query
+// row with the log-sum-exp weights and stores the output in the model dtype.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -42,22 +48,25 @@ namespace {
 
 constexpr int kKeys = 128;               // keys per chunk: the first product's M (TMEM lanes)
 constexpr int kQRows = 32;               // query rows per KV head, at most (TMEM columns per accumulator)
+constexpr int kWgRows = 16;              // query rows of one softmax warpgroup
 constexpr int kAttnStages = 3;           // chunks in the operand ring
-constexpr int kSoftThreads = 128;        // warps 0-3: softmax, one key / TMEM lane each
-constexpr int kProdThreads = 128;        // warps 4-7: producers, one key each
-constexpr int kAttnMmaWarp = 8;
-constexpr int kAttnThreads = 9 * 32;
+constexpr int kSoftWarps = 8;            // warps 0-7: softmax, two warpgroups of 16 query rows
+constexpr int kProdWarp0 = 8;            // warps 8-11: producers, one key per lane
+constexpr int kProdThreads = 128;
+constexpr int kAttnMmaWarp = 12;         // warp 12: MMA issue
+constexpr int kAttnThreads = 13 * 32;
 constexpr int kSplitGoal = 2048;         // context tokens per split aimed for
 constexpr int kMaxSplitTokens = 8192;
 constexpr int kWaveCtas = 152;           // stage-1 CTAs resident at once (one per SM of a GB300)
 constexpr int kCombineWarps = 8;
-constexpr uint32_t kAttnTmemCols = 128;  // S0 at column 0, S1 at 32, O at 64
+constexpr uint32_t kAttnTmemCols = 256;  // S0 at column 0, S1 at 32, O of key group w at 64 + 32 w
 constexpr uint64_t kAttnWaitNs = 2000000000ull;
 // A row's running maximum (log2 domain) is raised, and O and the sum
 // rescaled, only when a chunk's maximum exceeds it by more than this: the
 // weights stay below 2^8 (exact enough in the model dtype), and O seldom needs
 // the previous chunk's product to be complete.
 constexpr float kLazyRescale = 8.f;
+constexpr int64_t kNoKey = INT64_MIN;    // a key position past the context
 
 struct AttnPlan {
   int splits;
@@ -143,14 +152,16 @@ __host__ __device__ inline AttnLayout attn_layout(int D) {
   L.q_off = kAttnStages * L.stage_bytes;                   // Q: [D/64][32 rows][128 B]
   L.p_off = L.q_off + static_cast<uint32_t>(D / 64) * kQRows * 128;   // P^T: 2 x [2][32 rows][128 B]
   L.red_off = L.p_off + 2 * 2 * kQRows * 128;
-  L.bar_off = L.red_off + 2048;
+  L.bar_off = L.red_off + 4096;
   L.total = L.bar_off + 256 + 1024;                        // + alignment slack
   return L;
 }
 
 struct AttnBarriers {
-  uint64_t full[kAttnStages];
-  uint64_t empty[kAttnStages];
+  uint64_t full_k[kAttnStages];    // a chunk's K rows have landed
+  uint64_t full_v[kAttnStages];    // its V rows have landed
+  uint64_t empty_k[kAttnStages];   // its scores are computed: the K half is free
+  uint64_t empty_v[kAttnStages];   // its O product is done: the V half is free
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
@@ -159,7 +170,6 @@ struct AttnBarriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int rescale;     // some row's maximum grew in this chunk (O must be rescaled)
 };
 static_assert(sizeof(AttnBarriers) <= 256, "barrier area");
 
@@ -178,12 +188,12 @@ __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint3
 }
 
 // Transpose-reduction over a warp: on entry lane l holds v[j] = value of
-// (row l, column j); on exit v[0] of lane l is the reduction over the 32 rows
-// of column l.
+// (key l, row j) for 16 rows; on exit v[0] of lane l is the reduction over the
+// warp's 32 keys of row l % 16.
 template <bool kMax>
-__device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
+__device__ __forceinline__ float warp_rows16(float (&v)[16], int lane) {
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
+  for (int off = 8; off >= 1; off >>= 1) {
     const bool upper = (lane & off) != 0;
 #pragma unroll
     for (int i = 0; i < off; ++i) {
@@ -193,18 +203,47 @@ __device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
       v[i] = kMax ? fmaxf(keep, other) : keep + other;
     }
   }
-  return v[0];
+  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return kMax ? fmaxf(v[0], other) : v[0] + other;
 }
+
+// Store 16 consecutive fp32 columns of this thread's TMEM lane and wait.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+
+// Named barrier over `count` threads that returns how many of them passed a
+// true predicate.
+__device__ __forceinline__ uint32_t named_barrier_popc(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.popc.u32 %0, %2, %3, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r;
+}
+
+// The mbarrier's pending count drops by one when every asynchronous copy
+// this thread issued before has landed (the init count includes it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 16-byte-aligned zeros: the source of the rows of keys without a valid slot.
+__device__ __align__(16) uint8_t g_attn_zero_row[256];
 
 __device__ __forceinline__ void attn_flag(const AttnParams& p, uint32_t bits) {
   if (p.status != nullptr) atomicOr(p.status, bits);
 }
 
-__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -216,16 +255,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const AttnLayout L = attn_layout(D);
   AttnBarriers* bars = reinterpret_cast<AttnBarriers*>(smem + L.bar_off);
-  float* red_max = reinterpret_cast<float*>(smem + L.red_off);          // [4][32]
-  float* red_sum = red_max + 4 * 32;                                     // [4][32]
-  float* m_new = red_sum + 4 * 32;                                       // [32]
-  float* alpha_s = m_new + 32;                                           // [32]
+  float* alpha_s = reinterpret_cast<float*>(smem + L.red_off);   // [2 parity][2 wg][4 groups][16 rows]
+  int* resc_s = reinterpret_cast<int*>(alpha_s + 2 * 2 * 4 * kWgRows);   // [2 parity][2 wg][4 groups]
+  float* ml_s = reinterpret_cast<float*>(resc_s + 2 * 2 * 4);    // [2 wg][4 groups][16 rows][2]
   volatile int* abort_flag = &bars->abort;
   constexpr int kBlocksD = D / 64;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // the KV heads of one (request, split) are adjacent CTAs, so that the
-  // pieces they read of the same pool rows are requested close in time
+  // the KV heads of one (request, split) are adjacent CTAs
   const int64_t b = blockIdx.z;
   const int g = blockIdx.x;
   const int s = blockIdx.y;
@@ -247,23 +284,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
   if (!has_ext && n_ctx == 0) return;            // nothing in this split (uniform)
   const int ctx_chunks = (n_ctx + kKeys - 1) / kKeys;
   const int n_chunks = ctx_chunks + (has_ext ? 1 : 0);
+  const int nwg = p.rows / kWgRows;              // softmax warpgroups with rows (1 or 2)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAttnStages; ++i) {
-      mbar_init(smem_u32(&bars->full[i]), kProdThreads);
-      mbar_init(smem_u32(&bars->empty[i]), 1);
+      mbar_init(smem_u32(&bars->full_k[i]), kProdThreads);
+      mbar_init(smem_u32(&bars->full_v[i]), kProdThreads);
+      mbar_init(smem_u32(&bars->empty_k[i]), 1);
+      mbar_init(smem_u32(&bars->empty_v[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->s_full[i]), 1);
-      mbar_init(smem_u32(&bars->s_free[i]), kSoftThreads / 32);
-      mbar_init(smem_u32(&bars->p_full[i]), 1);
+      mbar_init(smem_u32(&bars->s_free[i]), 4 * nwg);
+      mbar_init(smem_u32(&bars->p_full[i]), 4 * nwg);
+      mbar_init(smem_u32(&bars->pv_done[i]), 1);
     }
-    mbar_init(smem_u32(&bars->pv_done[0]), 1);
-    mbar_init(smem_u32(&bars->pv_done[1]), 1);
     mbar_init(smem_u32(&bars->q_full), kProdThreads);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
-    bars->rescale = 0;
     fence_barrier_init();
   }
   if (warp == kAttnMmaWarp) {
@@ -275,9 +313,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
 
-  if (warp >= 4 && warp < 8) {
+  if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdThreads / 32) {
     // ------------------------------------------------------------ producers
-    const int pt = threadIdx.x - kSoftThreads;   // 0..127 among the producers
+    // Every copy is a 16-byte asynchronous copy; the mbarrier of a half stage
+    // (K or V rows of a chunk) completes when all 128 producer threads' copies
+    // issued before their arrival on it have landed, so nothing here waits
+    // for its own copies and up to three chunks are in flight.
+    const int pt = threadIdx.x - kProdWarp0 * 32;   // 0..127 among the producers
     const int pw = pt / 32;                         // producer warp
     const E* q = static_cast<const E*>(p.q);
     // Q of head g: row r = i*group + hh, its D columns as D/64 128-byte rows
@@ -287,142 +329,140 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       const uint32_t dst = smem_u32(smem + L.q_off) + (u / 8) * (kQRows * 128) + r * 128 + (((u % 8) ^ (r & 7)) * 16);
       cp_async16(dst, src);
     }
-    cp_async_commit_group();
+    cp_async_arrive_noinc(smem_u32(&bars->q_full));
+    // Warp pw copies keys 32*pw .. 32*pw+31 of a chunk; lane l learns the
+    // slot of key 32*pw + l two chunks ahead (the index load's latency under
+    // the gather's DRAM load exceeds a chunk).  A warp instruction covers whole
+    // K (or V) rows of 32 / (D/8) consecutive keys.  A key without a valid
+    // slot gets zero rows (its weight is 0, and 0 x NaN would not be).
+    constexpr int kUnits = D / 8;                 // 16-byte units of one head row
+    constexpr int kPerIter = 32 / kUnits;         // keys per warp instruction
+    const int sub = lane / kUnits, u = lane % kUnits;
+    // slot of key 32*pw + lane of chunk c (issued here, checked where used),
+    // kNoKey past the context, or the row of the block's own key
+    auto lane_slot = [&](int c) -> int64_t {
+      const int key = 32 * pw + lane;
+      if (c >= n_chunks) return kNoKey;
+      if (c < ctx_chunks) {
+        const int64_t t = lo + static_cast<int64_t>(c) * kKeys + key;
+        return t < hi ? p.kv_indices[k0 + t] : kNoKey;
+      }
+      return key < p.block ? b * p.block + key : kNoKey;
+    };
+    int64_t slot_cur = lane_slot(0), slot_nxt = lane_slot(1);
     bool ok_run = true;
     for (int c = 0; c < n_chunks && ok_run; ++c) {
       const int st = c % kAttnStages;
-      if (c >= kAttnStages &&
-          !mbar_wait(smem_u32(&bars->empty[st]), static_cast<uint32_t>(c / kAttnStages - 1) & 1u, abort_flag,
-                     kAttnWaitNs)) {
-        ok_run = false;
-        break;
-      }
-      // Warp pw copies keys 32*pw .. 32*pw+31 of the chunk.  Lane l learns the
-      // slot of key 32*pw + l; then the warp copies its keys one (D = 128) or
-      // two (D = 64) at a time, the lanes taking consecutive 16-byte units of
-      // the key's K row and then its V row, so that every copy instruction
-      // reads whole contiguous row segments.
-      int64_t my_k, my_v;   // element offsets of this lane's key's rows (K pool / K ext space)
-      bool my_ok;
-      {
-        const int key = 32 * pw + lane;
-        if (c < ctx_chunks) {
-          const int64_t t = lo + static_cast<int64_t>(c) * kKeys + key;
-          my_ok = t < hi;
-          int64_t slot = my_ok ? p.kv_indices[k0 + t] : 0;
-          if (my_ok && (slot < 0 || slot >= p.pool_slots)) {
-            attn_flag(p, DSPARK_FLAG_LOC_RANGE);
-            my_ok = false;
-          }
-          if (!my_ok) slot = 0;
-          my_k = my_v = slot * p.pool_row_stride + g * D;
-        } else {
-          my_ok = key < p.block;
-          const int64_t row = b * p.block + (my_ok ? key : 0);
-          my_k = my_v = (row * p.nkv + g) * D;
-        }
-      }
-      const E* kbase = static_cast<const E*>(c < ctx_chunks ? p.k_pool : p.k_ext);
-      const E* vbase = static_cast<const E*>(c < ctx_chunks ? p.v_pool : p.v_ext);
-      uint8_t* kst = smem + st * L.stage_bytes;
-      constexpr int kUnits = D / 8;                 // 16-byte units of one head row
-      constexpr int kPerIter = 32 / (2 * kUnits);   // keys per warp instruction
-      const int sub = lane / (2 * kUnits), w = lane % (2 * kUnits);
-      const bool is_v = w >= kUnits;
-      const int u = is_v ? w - kUnits : w;
-#pragma unroll 4
-      for (int j = 0; j < 32; j += kPerIter) {
-        const int kl = j + sub;                     // key within the warp's 32
-        const int key = 32 * pw + kl;
-        const bool ok = __shfl_sync(0xffffffffu, my_ok, kl);
-        const int64_t off = __shfl_sync(0xffffffffu, is_v ? my_v : my_k, kl);
-        const uint32_t dst_off = (is_v ? L.v_off : 0u) + (u / 8) * (kKeys * 128) + key * 128 +
-                                 (((u % 8) ^ (key & 7)) * 16);
-        if (ok)
-          cp_async16(smem_u32(kst + dst_off), (is_v ? vbase : kbase) + off + u * 8);
+      const bool own = c >= ctx_chunks;
+      int64_t my_off = -1;
+      if (slot_cur != kNoKey) {
+        if (own)
+          my_off = (slot_cur * p.nkv + g) * D;
+        else if (slot_cur >= 0 && slot_cur < p.pool_slots)
+          my_off = slot_cur * p.pool_row_stride + g * D;
         else
-          // a masked key: finite zeros (its weight is 0, and 0 x NaN would not be)
-          *reinterpret_cast<uint4*>(kst + dst_off) = make_uint4(0u, 0u, 0u, 0u);
+          attn_flag(p, DSPARK_FLAG_LOC_RANGE);
       }
-      cp_async_commit_group();
-      // the previous group (Q for c = 0, else chunk c-1) has landed: make it
-      // visible to the tensor cores and release it
-      cp_async_wait_group<1>();
-      fence_proxy_async_smem();
-      if (c == 0)
-        mbar_arrive(smem_u32(&bars->q_full));
-      else
-        mbar_arrive(smem_u32(&bars->full[(c - 1) % kAttnStages]));
+      slot_cur = slot_nxt;
+      slot_nxt = lane_slot(c + 2);
+      uint8_t* kst = smem + st * L.stage_bytes;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint64_t* empty = half == 0 ? &bars->empty_k[st] : &bars->empty_v[st];
+        if (c >= kAttnStages &&
+            !mbar_wait(smem_u32(empty), static_cast<uint32_t>(c / kAttnStages - 1) & 1u, abort_flag, kAttnWaitNs)) {
+          ok_run = false;
+          break;
+        }
+        const E* base = static_cast<const E*>(half == 0 ? (own ? p.k_ext : p.k_pool) : (own ? p.v_ext : p.v_pool));
+        const uint32_t st_base = smem_u32(kst) + (half == 0 ? 0u : L.v_off);
+#pragma unroll 4
+        for (int j = 0; j < 32; j += kPerIter) {
+          const int kl = j + sub;                   // key within the warp's 32
+          const int key = 32 * pw + kl;
+          const int64_t off = __shfl_sync(0xffffffffu, my_off, kl);
+          const uint32_t dst = st_base + (u / 8) * (kKeys * 128) + key * 128 + (((u % 8) ^ (key & 7)) * 16);
+          cp_async16(dst, off >= 0 ? static_cast<const void*>(base + off + u * 8)
+                                   : static_cast<const void*>(g_attn_zero_row + u * 16));
+        }
+        cp_async_arrive_noinc(smem_u32(half == 0 ? &bars->full_k[st] : &bars->full_v[st]));
+      }
     }
-    cp_async_wait_group<0>();
-    fence_proxy_async_smem();
-    if (ok_run) {
-      if (n_chunks == 0) mbar_arrive(smem_u32(&bars->q_full));
-      else mbar_arrive(smem_u32(&bars->full[(n_chunks - 1) % kAttnStages]));
-    } else if (threadIdx.x == kSoftThreads) {
+    cp_async_wait_all();   // no copy outlives the CTA
+    if (!ok_run && pt == 0) {
       *abort_flag = 1;
       attn_flag(p, DSPARK_FLAG_TIMEOUT);
     }
   } else if (warp == kAttnMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // Issues whichever product is ready: the scores of the next chunk (landed,
+    // its S buffer read by the softmax two chunks back) or the O product of the
+    // oldest chunk whose P^T is written.  The four key groups of a chunk (32
+    // keys, one softmax warp each) accumulate into their own O^T.
     if (lane == 0) {
       const uint32_t idesc_s = f16_instr_desc(ab_format<E>(), kKeys, p.rows);
       const uint32_t idesc_pv = f16_instr_desc(ab_format<E>(), kKeys, p.rows) | (1u << 15);   // A MN-major
       const uint32_t q_addr = smem_u32(smem + L.q_off);
       const uint32_t p_addr = smem_u32(smem + L.p_off);
-      const uint32_t t_o = tmem_base + 2 * kQRows;
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, kAttnWaitNs);
+      fence_proxy_async_smem();   // the copies landed through the generic proxy; the MMAs read via the async one
       bool issued = false;
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(smem_u32(&bars->p_full[j & 1]), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
-                       kAttnWaitNs))
-          return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + (j % kAttnStages) * L.stage_bytes + L.v_off);
-        const uint32_t pb = p_addr + (j & 1) * (2 * kQRows * 128);
+      int next_s = 0, next_pv = 0;
+      uint64_t t0 = global_timer_ns();
+      for (uint32_t it = 1; ok && next_pv < n_chunks; ++it) {
+        bool progress = false;
+        if (next_s < n_chunks) {
+          const int c = next_s, st = c % kAttnStages;
+          if (mbar_try_wait(smem_u32(&bars->full_k[st]), static_cast<uint32_t>(c / kAttnStages) & 1u) &&
+              (c < 2 || mbar_try_wait(smem_u32(&bars->s_free[c & 1]), static_cast<uint32_t>((c >> 1) - 1) & 1u))) {
+            fence_proxy_async_smem();
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(smem + st * L.stage_bytes);
+            const uint32_t t_s = tmem_base + (c & 1) * kQRows;
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          // 16 keys: two 8-key groups of the V block (1024 bytes each); P^T
-          // rows hold 64 keys per 128-byte block
-          const uint64_t ad = sw128_mnmajor_desc(v_addr + kk * 2048, D == 128 ? kKeys * 128 : 0);
-          const uint64_t bd = sw128_kmajor_desc(pb + (kk / 4) * (kQRows * 128) + (kk % 4) * 32);
-          umma_f16(t_o, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int blk = 0; blk < kBlocksD; ++blk)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_f16(t_s, sw128_kmajor_desc(k_addr + blk * (kKeys * 128) + k * 32),
+                         sw128_kmajor_desc(q_addr + blk * (kQRows * 128) + k * 32), idesc_s,
+                         (blk != 0 || k != 0) ? 1u : 0u);
+            umma_commit(smem_u32(&bars->s_full[c & 1]));
+            umma_commit(smem_u32(&bars->empty_k[st]));
+            issued = true;
+            ++next_s;
+            progress = true;
+          }
         }
-        umma_commit(smem_u32(&bars->empty[j % kAttnStages]));
-        umma_commit(smem_u32(&bars->pv_done[j & 1]));
-        issued = true;
-        return true;
-      };
-      // The product of chunk c - 1 goes first: it releases that chunk's stage
-      // as soon as its softmax is done; the scores of chunk c follow once it
-      // has landed (the softmax warps reach chunk c only after chunk c - 1).
-      for (int c = 0; c < n_chunks && ok; ++c) {
-        if (c >= 1 && !issue_pv(c - 1)) {
+        if (next_pv < next_s) {
+          const int j = next_pv;
+          if (mbar_try_wait(smem_u32(&bars->p_full[j & 1]), static_cast<uint32_t>(j >> 1) & 1u) &&
+              mbar_try_wait(smem_u32(&bars->full_v[j % kAttnStages]), static_cast<uint32_t>(j / kAttnStages) & 1u)) {
+            fence_proxy_async_smem();
+            tc_fence_after();
+            const uint32_t v_addr = smem_u32(smem + (j % kAttnStages) * L.stage_bytes + L.v_off);
+            const uint32_t pb = p_addr + (j & 1) * (2 * kQRows * 128);
+#pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk) {
+              // 16 keys: two 8-key groups of the V block (1024 bytes each); P^T
+              // rows hold 64 keys per 128-byte block; key group kk / 2
+              const uint64_t ad = sw128_mnmajor_desc(v_addr + kk * 2048, D == 128 ? kKeys * 128 : 0);
+              const uint64_t bd = sw128_kmajor_desc(pb + (kk / 4) * (kQRows * 128) + (kk % 4) * 32);
+              umma_f16(tmem_base + 2 * kQRows + (kk / 2) * kQRows, ad, bd, idesc_pv,
+                       (j > 0 || (kk & 1) != 0) ? 1u : 0u);
+            }
+            umma_commit(smem_u32(&bars->empty_v[j % kAttnStages]));
+            umma_commit(smem_u32(&bars->pv_done[j & 1]));
+            issued = true;
+            ++next_pv;
+            progress = true;
+          }
+        }
+        if (progress) {
+          t0 = global_timer_ns();
+        } else if ((it & 63u) == 0u && (*abort_flag || global_timer_ns() - t0 > kAttnWaitNs)) {
           ok = false;
-          break;
         }
-        const int st = c % kAttnStages;
-        if (!mbar_wait(smem_u32(&bars->full[st]), static_cast<uint32_t>(c / kAttnStages) & 1u, abort_flag,
-                       kAttnWaitNs) ||
-            (c >= 2 && !mbar_wait(smem_u32(&bars->s_free[c & 1]), static_cast<uint32_t>((c >> 1) - 1) & 1u,
-                                  abort_flag, kAttnWaitNs))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + st * L.stage_bytes);
-        const uint32_t t_s = tmem_base + (c & 1) * kQRows;
-#pragma unroll
-        for (int blk = 0; blk < kBlocksD; ++blk)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_f16(t_s, sw128_kmajor_desc(k_addr + blk * (kKeys * 128) + k * 32),
-                     sw128_kmajor_desc(q_addr + blk * (kQRows * 128) + k * 32), idesc_s,
-                     (blk != 0 || k != 0) ? 1u : 0u);
-        issued = true;
-        umma_commit(smem_u32(&bars->s_full[c & 1]));
       }
-      if (ok && n_chunks > 0) ok = issue_pv(n_chunks - 1);
       if (!ok) {
         *abort_flag = 1;
         attn_flag(p, DSPARK_FLAG_TIMEOUT);
@@ -433,128 +473,171 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
         mbar_wait(smem_u32(&bars->drain), 0, &never, kAttnWaitNs);
       }
     }
-  } else {
+  } else if (warp < kSoftWarps && warp / 4 < nwg) {
     // ------------------------------------------------------------ softmax
-    const int k = threadIdx.x;                       // key of the chunk = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_o = tmem_base + lane_off + 2 * kQRows;
-    float m_run = -INFINITY, l_run = 0.f;            // warp 0, lane r: query row r
+    // Warpgroup wg owns query rows wg*16 .. wg*16+15; warp wq of it owns keys
+    // 32*wq .. 32*wq+31 of every chunk (TMEM lanes), one per thread, and keeps
+    // its own running maximum and sum per row (lane r and r + 16: row
+    // wg*16 + r) for its own O^T accumulator.  Per chunk the warps of a
+    // warpgroup meet once, to learn whose O must be rescaled (and whether a
+    // wait gave up: then all of them leave together).
+    const int wg = warp / 4, wq = warp % 4;
+    const int k = wq * 32 + lane;
+    const uint32_t bar_id = 1 + wg;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    float m_run = -INFINITY, l_run = 0.f;
     uint8_t* p_smem = smem + L.p_off;
     bool done_ok = true;
+    auto key_slot = [&](int c) -> int64_t {   // slot of this thread's key in context chunk c
+      if (c >= ctx_chunks) return 0;
+      const int64_t t = lo + static_cast<int64_t>(c) * kKeys + k;
+      return t < hi ? p.kv_indices[k0 + t] : -1;
+    };
+    int64_t slot_cur = key_slot(0), slot_nxt = key_slot(1);   // loaded two chunks early
     for (int c = 0; c < n_chunks; ++c) {
-      const bool got = mbar_wait(smem_u32(&bars->s_full[c & 1]), static_cast<uint32_t>(c >> 1) & 1u, abort_flag,
-                                 kAttnWaitNs);
-      if (!named_barrier_and(1, kSoftThreads, got)) {
-        done_ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sraw[32];
-      tmem_ld32(tmem_base + lane_off + (c & 1) * kQRows, sraw);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[c & 1]));
+      const int par = c & 1;
       bool valid;
-      if (c < ctx_chunks) {
-        const int64_t t = lo + static_cast<int64_t>(c) * kKeys + k;
-        valid = t < hi;
-        if (valid) {
-          const int64_t slot = p.kv_indices[k0 + t];
-          valid = slot >= 0 && slot < p.pool_slots;
-        }
-      } else {
+      if (c < ctx_chunks)
+        valid = slot_cur >= 0 && slot_cur < p.pool_slots;
+      else
         valid = k < p.block;
-      }
-      float x[32];
+      slot_cur = slot_nxt;
+      slot_nxt = key_slot(c + 2);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[par]), static_cast<uint32_t>(c >> 1) & 1u,
+                                                  abort_flag, kAttnWaitNs));
+      bool grow = false;
+      if (ok) {
+        tc_fence_after();
+        uint32_t sraw[16];
+        tmem_ld16(tmem_base + lane_off + par * kQRows + wg * kWgRows, sraw);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[par]));
+        float x[16];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) x[r] = (valid && r < p.rows) ? __uint_as_float(sraw[r]) * p.scale_log2 : -INFINITY;
-      {
-        float t[32];
+        for (int r = 0; r < 16; ++r) x[r] = valid ? __uint_as_float(sraw[r]) * p.scale_log2 : -INFINITY;
+        float cm;
+        {
+          float t[16];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) t[r] = x[r];
-        red_max[warp * 32 + lane] = warp_columns<true>(t, lane);
-      }
-      named_barrier(1, kSoftThreads);
-      if (warp == 0) {
-        float cm = red_max[lane];
-#pragma unroll
-        for (int w = 1; w < 4; ++w) cm = fmaxf(cm, red_max[w * 32 + lane]);
+          for (int r = 0; r < 16; ++r) t[r] = x[r];
+          cm = warp_rows16<true>(t, lane);   // this warp's maximum of row lane % 16
+        }
         float al = 1.f;
-        if (cm > m_run + kLazyRescale) {   // also the first finite maximum (m_run = -inf)
+        if (cm > m_run + kLazyRescale) {     // also the first finite maximum (m_run = -inf)
           al = m_run == -INFINITY ? 1.f : exp2f(m_run - cm);
           m_run = cm;
         }
-        m_new[lane] = m_run;
-        alpha_s[lane] = al;
-        const bool grow = __any_sync(0xffffffffu, al != 1.f);
-        if (lane == 0) bars->rescale = grow ? 1 : 0;
-      }
-      named_barrier(1, kSoftThreads);
-      const bool rescale = bars->rescale != 0;
-      float pr[32];
+        grow = __any_sync(0xffffffffu, al != 1.f);
+        float pr[16];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        const float mr = m_new[r];
-        pr[r] = (x[r] == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(x[r] - mr);
-      }
-      // P buffer c & 1 was read by the product of chunk c - 2
-      bool pv_ok = c < 2 || mbar_wait(smem_u32(&bars->pv_done[c & 1]), static_cast<uint32_t>((c >> 1) - 1) & 1u,
-                                      abort_flag, kAttnWaitNs);
-      // P^T[row][key] in the model dtype: row r of block k/64, 16-byte unit
-      // (k%64)/8 XOR-swizzled by the row
-      uint8_t* pb = p_smem + (c & 1) * (2 * kQRows * 128) + (k / 64) * (kQRows * 128) + (k % 8) * 2;
-      if (pv_ok) {
+        for (int r = 0; r < 16; ++r) {
+          const float mr = __shfl_sync(0xffffffffu, m_run, r);
+          pr[r] = (x[r] == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(x[r] - mr);
+        }
+        // P buffer par was read by the product of chunk c - 2
+        ok = c < 2 || __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[par]),
+                                                        static_cast<uint32_t>((c >> 1) - 1) & 1u, abort_flag,
+                                                        kAttnWaitNs));
+        if (ok) {
+          // P^T[row][key] in the model dtype: row R of block k/64, 16-byte
+          // unit (k%64)/8 XOR-swizzled by the row
+          uint8_t* pb = p_smem + par * (2 * kQRows * 128) + (k / 64) * (kQRows * 128) + (k % 8) * 2;
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          *reinterpret_cast<uint16_t*>(pb + r * 128 + ((((k % 64) / 8) ^ (r & 7)) * 16)) = to_bits<E>(pr[r]);
+          for (int r = 0; r < 16; ++r) {
+            const int R = wg * kWgRows + r;
+            *reinterpret_cast<uint16_t*>(pb + R * 128 + ((((k % 64) / 8) ^ (R & 7)) * 16)) = to_bits<E>(pr[r]);
+          }
+        }
+        const float sum = warp_rows16<false>(pr, lane);
+        l_run = l_run * al + sum;
+        // a warp whose maximum grew publishes its factors; its accumulator may
+        // be rescaled once the previous chunk's product is complete
+        if (lane < 16) alpha_s[((par * 2 + wg) * 4 + wq) * kWgRows + lane] = al;
+        if (ok && grow && c >= 1)
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[(c - 1) & 1]),
+                                                 static_cast<uint32_t>((c - 1) >> 1) & 1u, abort_flag, kAttnWaitNs));
       }
-      red_sum[warp * 32 + lane] = warp_columns<false>(pr, lane);
-      // O is rescaled only once the previous chunk's product is complete
-      if (pv_ok && rescale && c >= 1)
-        pv_ok = mbar_wait(smem_u32(&bars->pv_done[(c - 1) & 1]), static_cast<uint32_t>((c - 1) >> 1) & 1u,
-                          abort_flag, kAttnWaitNs);
-      if (!named_barrier_and(1, kSoftThreads, pv_ok)) {
+      if (lane == 0) {
+        resc_s[(par * 2 + wg) * 4 + wq] = (ok && grow) ? 1 : 0;
+        if (!ok) *abort_flag = 1;   // the MMA issuer and the producers stop too
+      }
+      if (named_barrier_popc(bar_id, 128, !ok) != 0) {
         done_ok = false;
         break;
       }
-      if (warp == 0) {
-        float add = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) add += red_sum[w * 32 + lane];
-        l_run = l_run * alpha_s[lane] + add;
-      }
-      if (c >= 1 && rescale) {
+      if (c >= 1) {
+        // every warp rescales the grown accumulators over its own TMEM lanes
         tc_fence_after();
-        uint32_t o[32];
-        tmem_ld32(t_o, o);
+#pragma unroll 1
+        for (int w = 0; w < 4; ++w) {
+          if (resc_s[(par * 2 + wg) * 4 + w] == 0) continue;
+          const uint32_t t_ow = tmem_base + lane_off + 2 * kQRows + w * kQRows + wg * kWgRows;
+          uint32_t o[16];
+          tmem_ld16(t_ow, o);
 #pragma unroll
-        for (int r = 0; r < 32; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha_s[r]);
-        tmem_st32(t_o, o);
+          for (int r = 0; r < 16; ++r)
+            o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha_s[((par * 2 + wg) * 4 + w) * kWgRows + r]);
+          tmem_st16(t_ow, o);
+        }
       }
       fence_proxy_async_smem();   // P^T (generic stores) before the tensor cores read it
       tc_fence_before();
-      named_barrier(1, kSoftThreads);
-      if (k == 0) mbar_arrive(smem_u32(&bars->p_full[c & 1]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[par]));
     }
-    // ---- this split's unnormalised O^T, maximum and sum of every query row
-    if (done_ok && n_chunks > 0) {
-      done_ok = mbar_wait(smem_u32(&bars->pv_done[(n_chunks - 1) & 1]),
-                          static_cast<uint32_t>((n_chunks - 1) >> 1) & 1u, abort_flag, kAttnWaitNs);
-      done_ok = named_barrier_and(1, kSoftThreads, done_ok);
+    // ---- merge the four key groups' partial results of each row: this
+    // split's unnormalised O^T, maximum and sum of the warpgroup's rows
+    if (done_ok && n_chunks > 0)
+      done_ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[(n_chunks - 1) & 1]),
+                                                  static_cast<uint32_t>((n_chunks - 1) >> 1) & 1u, abort_flag,
+                                                  kAttnWaitNs));
+    if (lane < 16) {
+      ml_s[((wg * 4 + wq) * kWgRows + lane) * 2] = m_run;
+      ml_s[((wg * 4 + wq) * kWgRows + lane) * 2 + 1] = l_run;
     }
+    done_ok = named_barrier_and(bar_id, 128, done_ok);
     if (done_ok) {
       tc_fence_after();
-      uint32_t o[32];
-      tmem_ld32(t_o, o);
+      float acc[16], mmax[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float m = ml_s[((wg * 4) * kWgRows + r) * 2];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) m = fmaxf(m, ml_s[((wg * 4 + w) * kWgRows + r) * 2]);
+        mmax[r] = m;
+        acc[r] = 0.f;
+      }
+#pragma unroll 1
+      for (int w = 0; w < 4; ++w) {
+        uint32_t o[16];
+        tmem_ld16(tmem_base + lane_off + 2 * kQRows + w * kQRows + wg * kWgRows, o);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const float mw = ml_s[((wg * 4 + w) * kWgRows + r) * 2];
+          const float f = mw == -INFINITY ? 0.f : exp2f(mw - mmax[r]);
+          acc[r] += f * __uint_as_float(o[r]);
+        }
+      }
       const int nrows = p.nkv * p.rows;
-      const int64_t row0 = (b * p.splits + s) * static_cast<int64_t>(nrows) + static_cast<int64_t>(g) * p.rows;
+      const int64_t row0 = (b * p.splits + s) * static_cast<int64_t>(nrows) + static_cast<int64_t>(g) * p.rows +
+                           wg * kWgRows;
       if (k < D) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          if (r < p.rows) p.ws_o[(row0 + r) * D + k] = __uint_as_float(o[r]);
+        for (int r = 0; r < 16; ++r) p.ws_o[(row0 + r) * D + k] = acc[r];
       }
-      if (warp == 0 && lane < p.rows)
-        *reinterpret_cast<float2*>(p.ws_ml + (row0 + lane) * 2) = make_float2(m_run, l_run);
+      if (wq == 0 && lane < 16) {
+        float mrow = ml_s[((wg * 4) * kWgRows + lane) * 2];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) mrow = fmaxf(mrow, ml_s[((wg * 4 + w) * kWgRows + lane) * 2]);
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float mw = ml_s[((wg * 4 + w) * kWgRows + lane) * 2];
+          if (mw != -INFINITY) lsum += exp2f(mw - mrow) * ml_s[((wg * 4 + w) * kWgRows + lane) * 2 + 1];
+        }
+        *reinterpret_cast<float2*>(p.ws_ml + (row0 + lane) * 2) = make_float2(mrow, lsum);
+      }
     } else if (k == 0) {
       *abort_flag = 1;
       attn_flag(p, DSPARK_FLAG_TIMEOUT);
