@@ -15,9 +15,11 @@
 // head g (its K and V rows of the pool, or of the block's own keys for the
 // last chunk of split 0) with 16-byte asynchronous copies into the
 // 128-byte-swizzled layout of the MMA operands, three stages deep, a warp
-// instruction covering a key's whole rows; the staged chunk is the K-major A
-// operand of the first product and, read as an MN-major operand, the V^T of
-// the second.  Eight softmax warps, two warpgroups of 16 query rows, own one
+// instruction covering whole rows; the copies complete on mbarriers of the K
+// and V halves of a stage (the K half is free again once the scores are
+// computed), and slot indices are loaded two chunks ahead.  The staged chunk
+// is the K-major A operand of the first product and, read as an MN-major
+// operand, the V^T of the second.  Sixteen softmax warps, four warpgroups of 8 query rows, own one
 // key (TMEM lane) per thread.  Each warp keeps its own running maximum and
 // sum per row over its 32 keys of every chunk (warp transpose-reductions, no
 // exchange with the other warps), writes P^T (model dtype) to shared memory as
@@ -48,13 +50,15 @@ namespace {
 
 constexpr int kKeys = 128;               // keys per chunk: the first product's M (TMEM lanes)
 constexpr int kQRows = 32;               // query rows per KV head, at most (TMEM columns per accumulator)
-constexpr int kWgRows = 16;              // query rows of one softmax warpgroup
+constexpr int kWgRows = 8;               // query rows of one softmax warpgroup
 constexpr int kAttnStages = 3;           // chunks in the operand ring
-constexpr int kSoftWarps = 8;            // warps 0-7: softmax, two warpgroups of 16 query rows
-constexpr int kProdWarp0 = 8;            // warps 8-11: producers, one key per lane
-constexpr int kProdThreads = 128;
-constexpr int kAttnMmaWarp = 12;         // warp 12: MMA issue
-constexpr int kAttnThreads = 13 * 32;
+constexpr int kSoftWarps = 16;           // warps 0-15: softmax, four warpgroups of 8 query rows
+constexpr int kProdWarp0 = kSoftWarps;   // then the producers
+constexpr int kProdWarps = 4;
+constexpr int kProdThreads = kProdWarps * 32;
+constexpr int kKeysPerProdWarp = kKeys / kProdWarps;
+constexpr int kAttnMmaWarp = kProdWarp0 + kProdWarps;   // the MMA issuer
+constexpr int kAttnThreads = (kAttnMmaWarp + 1) * 32;
 constexpr int kSplitGoal = 2048;         // context tokens per split aimed for
 constexpr int kMaxSplitTokens = 8192;
 constexpr int kWaveCtas = 152;           // stage-1 CTAs resident at once (one per SM of a GB300)
@@ -188,12 +192,12 @@ __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint3
 }
 
 // Transpose-reduction over a warp: on entry lane l holds v[j] = value of
-// (key l, row j) for 16 rows; on exit v[0] of lane l is the reduction over the
-// warp's 32 keys of row l % 16.
-template <bool kMax>
-__device__ __forceinline__ float warp_rows16(float (&v)[16], int lane) {
+// (key l, row j) for R rows; on exit the result of lane l is the reduction
+// over the warp's 32 keys of row l % R.
+template <bool kMax, int R>
+__device__ __forceinline__ float warp_rows(float (&v)[R], int lane) {
 #pragma unroll
-  for (int off = 8; off >= 1; off >>= 1) {
+  for (int off = R / 2; off >= 1; off >>= 1) {
     const bool upper = (lane & off) != 0;
 #pragma unroll
     for (int i = 0; i < off; ++i) {
@@ -203,18 +207,53 @@ __device__ __forceinline__ float warp_rows16(float (&v)[16], int lane) {
       v[i] = kMax ? fmaxf(keep, other) : keep + other;
     }
   }
-  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
-  return kMax ? fmaxf(v[0], other) : v[0] + other;
+  float r = v[0];
+#pragma unroll
+  for (int off = R; off < 32; off <<= 1) {
+    const float other = __shfl_xor_sync(0xffffffffu, r, off);
+    r = kMax ? fmaxf(r, other) : r + other;
+  }
+  return r;
 }
 
-// Store 16 consecutive fp32 columns of this thread's TMEM lane and wait.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// 8 consecutive fp32 columns of this thread's TMEM lane (32x32b shape),
+// loaded and waited for in one statement.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr));
+}
+
+// Four runs of 8 columns, one wait: all four loads in flight together.
+#define DSPARK_O8(a, i) "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7])
+__device__ __forceinline__ void tmem_ld8x4(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, uint32_t (&a)[8],
+                                           uint32_t (&b)[8], uint32_t (&c)[8], uint32_t (&d)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%33];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%34];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%35];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : DSPARK_O8(a, 0), DSPARK_O8(b, 0), DSPARK_O8(c, 0), DSPARK_O8(d, 0)
+      : "r"(t0), "r"(t1), "r"(t2), "r"(t3));
+}
+#undef DSPARK_O8
+
+// Store 8 consecutive fp32 columns of this thread's TMEM lane and wait.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
       "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
+}
+
+// 2^x (PTX ex2.approx.ftz: relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Named barrier over `count` threads that returns how many of them passed a
@@ -255,9 +294,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const AttnLayout L = attn_layout(D);
   AttnBarriers* bars = reinterpret_cast<AttnBarriers*>(smem + L.bar_off);
-  float* alpha_s = reinterpret_cast<float*>(smem + L.red_off);   // [2 parity][2 wg][4 groups][16 rows]
-  int* resc_s = reinterpret_cast<int*>(alpha_s + 2 * 2 * 4 * kWgRows);   // [2 parity][2 wg][4 groups]
-  float* ml_s = reinterpret_cast<float*>(resc_s + 2 * 2 * 4);    // [2 wg][4 groups][16 rows][2]
+  constexpr int kWgs = kSoftWarps / 4;
+  float* alpha_s = reinterpret_cast<float*>(smem + L.red_off);   // [2 parity][kWgs][4 groups][kWgRows]
+  int* resc_s = reinterpret_cast<int*>(alpha_s + 2 * kWgs * 4 * kWgRows);   // [2 parity][kWgs][4 groups]
+  float* ml_s = reinterpret_cast<float*>(resc_s + 2 * kWgs * 4);    // [kWgs][4 groups][kWgRows][2]
   volatile int* abort_flag = &bars->abort;
   constexpr int kBlocksD = D / 64;
 
@@ -284,7 +324,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
   if (!has_ext && n_ctx == 0) return;            // nothing in this split (uniform)
   const int ctx_chunks = (n_ctx + kKeys - 1) / kKeys;
   const int n_chunks = ctx_chunks + (has_ext ? 1 : 0);
-  const int nwg = p.rows / kWgRows;              // softmax warpgroups with rows (1 or 2)
+  const int nwg = p.rows / kWgRows;              // softmax warpgroups with rows (2 or 4)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAttnStages; ++i) {
@@ -330,19 +370,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       cp_async16(dst, src);
     }
     cp_async_arrive_noinc(smem_u32(&bars->q_full));
-    // Warp pw copies keys 32*pw .. 32*pw+31 of a chunk; lane l learns the
-    // slot of key 32*pw + l two chunks ahead (the index load's latency under
+    // Warp pw copies kKeysPerProdWarp keys of a chunk; lane l learns the
+    // slot of its key l two chunks ahead (the index load's latency under
     // the gather's DRAM load exceeds a chunk).  A warp instruction covers whole
     // K (or V) rows of 32 / (D/8) consecutive keys.  A key without a valid
     // slot gets zero rows (its weight is 0, and 0 x NaN would not be).
     constexpr int kUnits = D / 8;                 // 16-byte units of one head row
     constexpr int kPerIter = 32 / kUnits;         // keys per warp instruction
     const int sub = lane / kUnits, u = lane % kUnits;
-    // slot of key 32*pw + lane of chunk c (issued here, checked where used),
-    // kNoKey past the context, or the row of the block's own key
+    // slot of key kKeysPerProdWarp*pw + lane of chunk c (issued here, checked
+    // where used), kNoKey past the context, or the row of the block's own key
     auto lane_slot = [&](int c) -> int64_t {
-      const int key = 32 * pw + lane;
-      if (c >= n_chunks) return kNoKey;
+      const int key = kKeysPerProdWarp * pw + lane;
+      if (c >= n_chunks || lane >= kKeysPerProdWarp) return kNoKey;
       if (c < ctx_chunks) {
         const int64_t t = lo + static_cast<int64_t>(c) * kKeys + key;
         return t < hi ? p.kv_indices[k0 + t] : kNoKey;
@@ -377,9 +417,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
         const E* base = static_cast<const E*>(half == 0 ? (own ? p.k_ext : p.k_pool) : (own ? p.v_ext : p.v_pool));
         const uint32_t st_base = smem_u32(kst) + (half == 0 ? 0u : L.v_off);
 #pragma unroll 4
-        for (int j = 0; j < 32; j += kPerIter) {
-          const int kl = j + sub;                   // key within the warp's 32
-          const int key = 32 * pw + kl;
+        for (int j = 0; j < kKeysPerProdWarp; j += kPerIter) {
+          const int kl = j + sub;                   // key within the warp's share
+          const int key = kKeysPerProdWarp * pw + kl;
           const int64_t off = __shfl_sync(0xffffffffu, my_off, kl);
           const uint32_t dst = st_base + (u / 8) * (kKeys * 128) + key * 128 + (((u % 8) ^ (key & 7)) * 16);
           cp_async16(dst, off >= 0 ? static_cast<const void*>(base + off + u * 8)
@@ -475,12 +515,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
     }
   } else if (warp < kSoftWarps && warp / 4 < nwg) {
     // ------------------------------------------------------------ softmax
-    // Warpgroup wg owns query rows wg*16 .. wg*16+15; warp wq of it owns keys
-    // 32*wq .. 32*wq+31 of every chunk (TMEM lanes), one per thread, and keeps
-    // its own running maximum and sum per row (lane r and r + 16: row
-    // wg*16 + r) for its own O^T accumulator.  Per chunk the warps of a
+    // Warpgroup wg owns query rows wg*R .. wg*R+R-1 (R = kWgRows); warp wq of
+    // it owns keys 32*wq .. 32*wq+31 of every chunk (TMEM lanes), one per
+    // thread, and keeps its own running maximum and sum per row (lane l: row
+    // wg*R + l % R) for its own O^T accumulator.  Per chunk the warps of a
     // warpgroup meet once, to learn whose O must be rescaled (and whether a
     // wait gave up: then all of them leave together).
+    constexpr int R = kWgRows;
     const int wg = warp / 4, wq = warp % 4;
     const int k = wq * 32 + lane;
     const uint32_t bar_id = 1 + wg;
@@ -508,58 +549,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       bool grow = false;
       if (ok) {
         tc_fence_after();
-        uint32_t sraw[16];
-        tmem_ld16(tmem_base + lane_off + par * kQRows + wg * kWgRows, sraw);
+        uint32_t sraw[R];
+        tmem_ld8(tmem_base + lane_off + par * kQRows + wg * R, sraw);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[par]));
-        float x[16];
+        float x[R];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = valid ? __uint_as_float(sraw[r]) * p.scale_log2 : -INFINITY;
+        for (int r = 0; r < R; ++r) x[r] = valid ? __uint_as_float(sraw[r]) * p.scale_log2 : -INFINITY;
         float cm;
         {
-          float t[16];
+          float t[R];
 #pragma unroll
-          for (int r = 0; r < 16; ++r) t[r] = x[r];
-          cm = warp_rows16<true>(t, lane);   // this warp's maximum of row lane % 16
+          for (int r = 0; r < R; ++r) t[r] = x[r];
+          cm = warp_rows<true, R>(t, lane);   // this warp's maximum of row lane % R
         }
         float al = 1.f;
-        if (cm > m_run + kLazyRescale) {     // also the first finite maximum (m_run = -inf)
-          al = m_run == -INFINITY ? 1.f : exp2f(m_run - cm);
+        if (cm > m_run + kLazyRescale) {      // also the first finite maximum (m_run = -inf)
+          al = m_run == -INFINITY ? 1.f : fast_exp2(m_run - cm);
           m_run = cm;
         }
         grow = __any_sync(0xffffffffu, al != 1.f);
-        float pr[16];
+        float pr[R];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
+        for (int r = 0; r < R; ++r) {
           const float mr = __shfl_sync(0xffffffffu, m_run, r);
-          pr[r] = (x[r] == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(x[r] - mr);
+          pr[r] = (x[r] == -INFINITY || mr == -INFINITY) ? 0.f : fast_exp2(x[r] - mr);
         }
         // P buffer par was read by the product of chunk c - 2
         ok = c < 2 || __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[par]),
                                                         static_cast<uint32_t>((c >> 1) - 1) & 1u, abort_flag,
                                                         kAttnWaitNs));
         if (ok) {
-          // P^T[row][key] in the model dtype: row R of block k/64, 16-byte
+          // P^T[row][key] in the model dtype: row Rw of block k/64, 16-byte
           // unit (k%64)/8 XOR-swizzled by the row
           uint8_t* pb = p_smem + par * (2 * kQRows * 128) + (k / 64) * (kQRows * 128) + (k % 8) * 2;
 #pragma unroll
-          for (int r = 0; r < 16; ++r) {
-            const int R = wg * kWgRows + r;
-            *reinterpret_cast<uint16_t*>(pb + R * 128 + ((((k % 64) / 8) ^ (R & 7)) * 16)) = to_bits<E>(pr[r]);
+          for (int r = 0; r < R; ++r) {
+            const int Rw = wg * R + r;
+            *reinterpret_cast<uint16_t*>(pb + Rw * 128 + ((((k % 64) / 8) ^ (Rw & 7)) * 16)) = to_bits<E>(pr[r]);
           }
         }
-        const float sum = warp_rows16<false>(pr, lane);
+        const float sum = warp_rows<false, R>(pr, lane);
         l_run = l_run * al + sum;
         // a warp whose maximum grew publishes its factors; its accumulator may
         // be rescaled once the previous chunk's product is complete
-        if (lane < 16) alpha_s[((par * 2 + wg) * 4 + wq) * kWgRows + lane] = al;
+        if (lane < R) alpha_s[((par * kWgs + wg) * 4 + wq) * R + lane] = al;
         if (ok && grow && c >= 1)
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[(c - 1) & 1]),
                                                  static_cast<uint32_t>((c - 1) >> 1) & 1u, abort_flag, kAttnWaitNs));
       }
       if (lane == 0) {
-        resc_s[(par * 2 + wg) * 4 + wq] = (ok && grow) ? 1 : 0;
+        resc_s[(par * kWgs + wg) * 4 + wq] = (ok && grow) ? 1 : 0;
         if (!ok) *abort_flag = 1;   // the MMA issuer and the producers stop too
       }
       if (named_barrier_popc(bar_id, 128, !ok) != 0) {
@@ -568,17 +609,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       }
       if (c >= 1) {
         // every warp rescales the grown accumulators over its own TMEM lanes
-        tc_fence_after();
+        const int* rs = resc_s + (par * kWgs + wg) * 4;
+        if ((rs[0] | rs[1] | rs[2] | rs[3]) != 0) {
+          tc_fence_after();
 #pragma unroll 1
-        for (int w = 0; w < 4; ++w) {
-          if (resc_s[(par * 2 + wg) * 4 + w] == 0) continue;
-          const uint32_t t_ow = tmem_base + lane_off + 2 * kQRows + w * kQRows + wg * kWgRows;
-          uint32_t o[16];
-          tmem_ld16(t_ow, o);
+          for (int w = 0; w < 4; ++w) {
+            if (rs[w] == 0) continue;
+            const uint32_t t_ow = tmem_base + lane_off + 2 * kQRows + w * kQRows + wg * R;
+            uint32_t o[R];
+            tmem_ld8(t_ow, o);
 #pragma unroll
-          for (int r = 0; r < 16; ++r)
-            o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha_s[((par * 2 + wg) * 4 + w) * kWgRows + r]);
-          tmem_st16(t_ow, o);
+            for (int r = 0; r < R; ++r)
+              o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha_s[((par * kWgs + wg) * 4 + w) * R + r]);
+            tmem_st8(t_ow, o);
+          }
         }
       }
       fence_proxy_async_smem();   // P^T (generic stores) before the tensor cores read it
@@ -592,51 +636,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       done_ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[(n_chunks - 1) & 1]),
                                                   static_cast<uint32_t>((n_chunks - 1) >> 1) & 1u, abort_flag,
                                                   kAttnWaitNs));
-    if (lane < 16) {
-      ml_s[((wg * 4 + wq) * kWgRows + lane) * 2] = m_run;
-      ml_s[((wg * 4 + wq) * kWgRows + lane) * 2 + 1] = l_run;
+    if (lane < R) {
+      ml_s[((wg * 4 + wq) * R + lane) * 2] = m_run;
+      ml_s[((wg * 4 + wq) * R + lane) * 2 + 1] = l_run;
     }
     done_ok = named_barrier_and(bar_id, 128, done_ok);
     if (done_ok) {
       tc_fence_after();
-      float acc[16], mmax[16];
+      uint32_t o[4][R];
+      const uint32_t t_o = tmem_base + lane_off + 2 * kQRows + wg * R;
+      tmem_ld8x4(t_o, t_o + kQRows, t_o + 2 * kQRows, t_o + 3 * kQRows, o[0], o[1], o[2], o[3]);
+      float acc[R];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float m = ml_s[((wg * 4) * kWgRows + r) * 2];
+      for (int r = 0; r < R; ++r) {
+        float mw[4];
 #pragma unroll
-        for (int w = 1; w < 4; ++w) m = fmaxf(m, ml_s[((wg * 4 + w) * kWgRows + r) * 2]);
-        mmax[r] = m;
-        acc[r] = 0.f;
-      }
-#pragma unroll 1
-      for (int w = 0; w < 4; ++w) {
-        uint32_t o[16];
-        tmem_ld16(tmem_base + lane_off + 2 * kQRows + w * kQRows + wg * kWgRows, o);
+        for (int w = 0; w < 4; ++w) mw[w] = ml_s[((wg * 4 + w) * R + r) * 2];
+        const float m = fmaxf(fmaxf(mw[0], mw[1]), fmaxf(mw[2], mw[3]));
+        float a = 0.f;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const float mw = ml_s[((wg * 4 + w) * kWgRows + r) * 2];
-          const float f = mw == -INFINITY ? 0.f : exp2f(mw - mmax[r]);
-          acc[r] += f * __uint_as_float(o[r]);
-        }
+        for (int w = 0; w < 4; ++w)
+          if (mw[w] != -INFINITY) a += fast_exp2(mw[w] - m) * __uint_as_float(o[w][r]);
+        acc[r] = a;
       }
       const int nrows = p.nkv * p.rows;
       const int64_t row0 = (b * p.splits + s) * static_cast<int64_t>(nrows) + static_cast<int64_t>(g) * p.rows +
-                           wg * kWgRows;
+                           wg * R;
       if (k < D) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) p.ws_o[(row0 + r) * D + k] = acc[r];
+        for (int r = 0; r < R; ++r) p.ws_o[(row0 + r) * D + k] = acc[r];
       }
-      if (wq == 0 && lane < 16) {
-        float mrow = ml_s[((wg * 4) * kWgRows + lane) * 2];
+      if (wq == 0 && lane < R) {
+        float mw[4];
 #pragma unroll
-        for (int w = 1; w < 4; ++w) mrow = fmaxf(mrow, ml_s[((wg * 4 + w) * kWgRows + lane) * 2]);
+        for (int w = 0; w < 4; ++w) mw[w] = ml_s[((wg * 4 + w) * R + lane) * 2];
+        const float m = fmaxf(fmaxf(mw[0], mw[1]), fmaxf(mw[2], mw[3]));
         float lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float mw = ml_s[((wg * 4 + w) * kWgRows + lane) * 2];
-          if (mw != -INFINITY) lsum += exp2f(mw - mrow) * ml_s[((wg * 4 + w) * kWgRows + lane) * 2 + 1];
-        }
-        *reinterpret_cast<float2*>(p.ws_ml + (row0 + lane) * 2) = make_float2(mrow, lsum);
+        for (int w = 0; w < 4; ++w)
+          if (mw[w] != -INFINITY) lsum += fast_exp2(mw[w] - m) * ml_s[((wg * 4 + w) * R + lane) * 2 + 1];
+        *reinterpret_cast<float2*>(p.ws_ml + (row0 + lane) * 2) = make_float2(m, lsum);
       }
     } else if (k == 0) {
       *abort_flag = 1;
