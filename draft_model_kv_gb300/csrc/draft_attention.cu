@@ -279,6 +279,29 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 // 16-byte-aligned zeros: the source of the rows of keys without a valid slot.
 __device__ __align__(16) uint8_t g_attn_zero_row[256];
 
+// Wait until the phase with the given parity has completed; a waiting thread
+// sleeps in the barrier (up to kSuspendNs per try) instead of spinning, so the
+// roles that have work keep the issue slots.  Gives up (false) when *abort
+// becomes non-zero or after limit_ns.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 __device__ __forceinline__ void attn_flag(const AttnParams& p, uint32_t bits) {
   if (p.status != nullptr) atomicOr(p.status, bits);
 }
@@ -410,13 +433,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       for (int half = 0; half < 2; ++half) {
         uint64_t* empty = half == 0 ? &bars->empty_k[st] : &bars->empty_v[st];
         if (c >= kAttnStages &&
-            !mbar_wait(smem_u32(empty), static_cast<uint32_t>(c / kAttnStages - 1) & 1u, abort_flag, kAttnWaitNs)) {
+            !attn_wait(smem_u32(empty), static_cast<uint32_t>(c / kAttnStages - 1) & 1u, abort_flag, kAttnWaitNs)) {
           ok_run = false;
           break;
         }
         const E* base = static_cast<const E*>(half == 0 ? (own ? p.k_ext : p.k_pool) : (own ? p.v_ext : p.v_pool));
         const uint32_t st_base = smem_u32(kst) + (half == 0 ? 0u : L.v_off);
-#pragma unroll 4
+#pragma unroll
         for (int j = 0; j < kKeysPerProdWarp; j += kPerIter) {
           const int kl = j + sub;                   // key within the warp's share
           const int key = kKeysPerProdWarp * pw + kl;
@@ -444,7 +467,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       const uint32_t idesc_pv = f16_instr_desc(ab_format<E>(), kKeys, p.rows) | (1u << 15);   // A MN-major
       const uint32_t q_addr = smem_u32(smem + L.q_off);
       const uint32_t p_addr = smem_u32(smem + L.p_off);
-      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, kAttnWaitNs);
+      bool ok = attn_wait(smem_u32(&bars->q_full), 0, abort_flag, kAttnWaitNs);
       fence_proxy_async_smem();   // the copies landed through the generic proxy; the MMAs read via the async one
       bool issued = false;
       int next_s = 0, next_pv = 0;
@@ -510,7 +533,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       if (issued) {
         umma_commit(smem_u32(&bars->drain));
         int never = 0;
-        mbar_wait(smem_u32(&bars->drain), 0, &never, kAttnWaitNs);
+        attn_wait(smem_u32(&bars->drain), 0, &never, kAttnWaitNs);
       }
     }
   } else if (warp < kSoftWarps && warp / 4 < nwg) {
@@ -544,7 +567,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
         valid = k < p.block;
       slot_cur = slot_nxt;
       slot_nxt = key_slot(c + 2);
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[par]), static_cast<uint32_t>(c >> 1) & 1u,
+      bool ok = __all_sync(0xffffffffu, attn_wait(smem_u32(&bars->s_full[par]), static_cast<uint32_t>(c >> 1) & 1u,
                                                   abort_flag, kAttnWaitNs));
       bool grow = false;
       if (ok) {
@@ -556,13 +579,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
         if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[par]));
         float x[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) x[r] = valid ? __uint_as_float(sraw[r]) * p.scale_log2 : -INFINITY;
+        for (int r = 0; r < R; ++r) x[r] = valid ? __uint_as_float(sraw[r]) : -INFINITY;   // raw scores
         float cm;
         {
           float t[R];
 #pragma unroll
           for (int r = 0; r < R; ++r) t[r] = x[r];
-          cm = warp_rows<true, R>(t, lane);   // this warp's maximum of row lane % R
+          // this warp's maximum of row lane % R, in the scaled log2 domain
+          cm = warp_rows<true, R>(t, lane) * p.scale_log2;
         }
         float al = 1.f;
         if (cm > m_run + kLazyRescale) {      // also the first finite maximum (m_run = -inf)
@@ -574,10 +598,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const float mr = __shfl_sync(0xffffffffu, m_run, r);
-          pr[r] = (x[r] == -INFINITY || mr == -INFINITY) ? 0.f : fast_exp2(x[r] - mr);
+          pr[r] = (x[r] == -INFINITY || mr == -INFINITY) ? 0.f : fast_exp2(fmaf(x[r], p.scale_log2, -mr));
         }
         // P buffer par was read by the product of chunk c - 2
-        ok = c < 2 || __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[par]),
+        ok = c < 2 || __all_sync(0xffffffffu, attn_wait(smem_u32(&bars->pv_done[par]),
                                                         static_cast<uint32_t>((c >> 1) - 1) & 1u, abort_flag,
                                                         kAttnWaitNs));
         if (ok) {
@@ -596,7 +620,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
         // be rescaled once the previous chunk's product is complete
         if (lane < R) alpha_s[((par * kWgs + wg) * 4 + wq) * R + lane] = al;
         if (ok && grow && c >= 1)
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[(c - 1) & 1]),
+          ok = __all_sync(0xffffffffu, attn_wait(smem_u32(&bars->pv_done[(c - 1) & 1]),
                                                  static_cast<uint32_t>((c - 1) >> 1) & 1u, abort_flag, kAttnWaitNs));
       }
       if (lane == 0) {
@@ -633,7 +657,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
     // ---- merge the four key groups' partial results of each row: this
     // split's unnormalised O^T, maximum and sum of the warpgroup's rows
     if (done_ok && n_chunks > 0)
-      done_ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[(n_chunks - 1) & 1]),
+      done_ok = __all_sync(0xffffffffu, attn_wait(smem_u32(&bars->pv_done[(n_chunks - 1) & 1]),
                                                   static_cast<uint32_t>((n_chunks - 1) >> 1) & 1u, abort_flag,
                                                   kAttnWaitNs));
     if (lane < R) {
