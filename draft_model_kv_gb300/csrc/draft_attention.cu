@@ -400,6 +400,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
     // slot gets zero rows (its weight is 0, and 0 x NaN would not be).
     constexpr int kUnits = D / 8;                 // 16-byte units of one head row
     constexpr int kPerIter = 32 / kUnits;         // keys per warp instruction
+    constexpr int kXs = 8 / kPerIter;             // distinct swizzle rows of a lane's copies
     const int sub = lane / kUnits, u = lane % kUnits;
     // slot of key kKeysPerProdWarp*pw + lane of chunk c (issued here, checked
     // where used), kNoKey past the context, or the row of the block's own key
@@ -428,6 +429,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       }
       slot_cur = slot_nxt;
       slot_nxt = lane_slot(c + 2);
+      // the owner lane of each key resolves its K and V row pointers (the
+      // zero row for a key without a valid slot): a copy is then a shuffle, an
+      // add and the copy itself
+      uintptr_t my_k = reinterpret_cast<uintptr_t>(g_attn_zero_row), my_v = my_k;
+      if (my_off >= 0) {
+        my_k = reinterpret_cast<uintptr_t>(static_cast<const E*>(own ? p.k_ext : p.k_pool) + my_off);
+        my_v = reinterpret_cast<uintptr_t>(static_cast<const E*>(own ? p.v_ext : p.v_pool) + my_off);
+      }
       uint8_t* kst = smem + st * L.stage_bytes;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -437,16 +446,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
           ok_run = false;
           break;
         }
-        const E* base = static_cast<const E*>(half == 0 ? (own ? p.k_ext : p.k_pool) : (own ? p.v_ext : p.v_pool));
-        const uint32_t st_base = smem_u32(kst) + (half == 0 ? 0u : L.v_off);
+        const unsigned long long mine = half == 0 ? my_k : my_v;
+        // this lane's destinations: key kl = jj + sub of the warp's share, its
+        // 16-byte unit u at (kl & 7) ^ u in the row; (kl & 7) takes kXs values
+        const uint32_t lane_base = smem_u32(kst) + (half == 0 ? 0u : L.v_off) + (u / 8) * (kKeys * 128) +
+                                   (kKeysPerProdWarp * pw + sub) * 128;
+        uint32_t dst[kXs];
 #pragma unroll
-        for (int j = 0; j < kKeysPerProdWarp; j += kPerIter) {
-          const int kl = j + sub;                   // key within the warp's share
-          const int key = kKeysPerProdWarp * pw + kl;
-          const int64_t off = __shfl_sync(0xffffffffu, my_off, kl);
-          const uint32_t dst = st_base + (u / 8) * (kKeys * 128) + key * 128 + (((u % 8) ^ (key & 7)) * 16);
-          cp_async16(dst, off >= 0 ? static_cast<const void*>(base + off + u * 8)
-                                   : static_cast<const void*>(g_attn_zero_row + u * 16));
+        for (int q = 0; q < kXs; ++q) dst[q] = lane_base + (((u % 8) ^ ((q * kPerIter + sub) & 7)) * 16);
+#pragma unroll
+        for (int jj = 0; jj < kKeysPerProdWarp; jj += kPerIter) {
+          const unsigned long long src = __shfl_sync(0xffffffffu, mine, jj + sub) + static_cast<unsigned>(u * 16);
+          cp_async16(dst[(jj / kPerIter) % kXs] + jj * 128, reinterpret_cast<const void*>(src));
         }
         cp_async_arrive_noinc(smem_u32(half == 0 ? &bars->full_k[st] : &bars->full_v[st]));
       }
