@@ -19,7 +19,8 @@ from ._abi import (DSparkError, FLAG_LOC_RANGE, FLAG_POS_RANGE, FLAG_TIMEOUT,  #
 
 __all__ = [
     "DSparkError", "Layer", "Bundle", "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv",
-    "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_clear_device_status",
+    "dspark_write_ctx_kv", "dspark_get_device_status", "dspark_read_device_status_async",
+    "dspark_clear_device_status",
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc", "dspark_set_split_wait_test",
     "dspark_set_kernel_variant", "dspark_describe_schedule", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
     "dspark_correct_drafts_and_bonus", "dspark_draft_attention", "dspark_draft_attention_workspace_bytes",
@@ -222,6 +223,17 @@ def dspark_get_device_status(bundle: Bundle, stream=None) -> int:
     _abi.check(load().dspark_get_device_status(bundle.handle, _stream_handle(stream),
                                                ctypes.byref(flags)), "dspark_get_device_status")
     return flags.value
+
+
+def dspark_read_device_status_async(bundle: Bundle, out, stream=None) -> None:
+    """Enqueue on `stream` the copy of the bundle's status word into `out`, a
+    one-element int32/uint32 CPU tensor (pinned for a truly asynchronous
+    copy); read `out` only after synchronising the stream."""
+    import torch
+    if out.device.type != "cpu" or out.numel() < 1 or out.element_size() != 4 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU tensor of 4-byte elements")
+    _abi.check(load().dspark_read_device_status_async(bundle.handle, _stream_handle(stream), out.data_ptr()),
+               "dspark_read_device_status_async")
 
 
 def dspark_clear_device_status(bundle: Bundle, stream=None) -> None:

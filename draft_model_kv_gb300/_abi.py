@@ -33,7 +33,8 @@ CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTS = (
     "dspark_check_ctx_kv_layers", "dspark_pack_ctx_kv", "dspark_write_ctx_kv",
-    "dspark_get_device_status", "dspark_clear_device_status", "dspark_bundle_get_info",
+    "dspark_get_device_status", "dspark_read_device_status_async", "dspark_clear_device_status",
+    "dspark_bundle_get_info",
     "dspark_free_bundle", "dspark_status_string", "dspark_set_trace_buffer",
     "dspark_write_ctx_kv_noalloc", "dspark_set_kernel_variant", "dspark_describe_schedule",
     "dspark_set_split_wait_test",
@@ -97,6 +98,8 @@ def load() -> ctypes.CDLL:
     lib.dspark_write_ctx_kv.restype = ctypes.c_int
     lib.dspark_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.dspark_get_device_status.restype = ctypes.c_int
+    lib.dspark_read_device_status_async.argtypes = [vp, vp, vp]
+    lib.dspark_read_device_status_async.restype = ctypes.c_int
     lib.dspark_clear_device_status.argtypes = [vp, vp]
     lib.dspark_clear_device_status.restype = ctypes.c_int
     lib.dspark_bundle_get_info.argtypes = [vp, ctypes.POINTER(BundleInfo)]

@@ -251,6 +251,16 @@ DSPARK_API int dspark_write_ctx_kv_noalloc(
  * `stream`; synchronises `stream`. */
 DSPARK_API int dspark_get_device_status(dspark_bundle_t bundle, void* stream, uint32_t* flags /* (host) */);
 
+/* As dspark_get_device_status, without waiting: enqueue on `stream` the copy
+ * of the status word to *flags and return.  *flags must stay valid until the
+ * copy has run, and is meaningful only after `stream` (or an event recorded
+ * on it after this call) has been synchronised; for the copy to be truly
+ * asynchronous *flags should be page-locked host memory.  This lets a
+ * pipelined caller read every write's status without a synchronisation per
+ * write.  Returns DSPARK_E_INVALID_ARG for a NULL bundle or flags, else
+ * DSPARK_OK or DSPARK_E_CUDA (enqueueing failed). */
+DSPARK_API int dspark_read_device_status_async(dspark_bundle_t bundle, void* stream, uint32_t* flags /* (host) */);
+
 /* Reset the device status word to 0 and the split-tile arrival counters
  * (stream-ordered, asynchronous).  Call it after a write that reported
  * DSPARK_FLAG_TIMEOUT: such a write may leave counters set. */

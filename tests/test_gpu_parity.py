@@ -285,6 +285,12 @@ def test_out_of_range_position_and_loc_are_flagged_and_skipped():
     dk.dspark_clear_device_status(b)
     dk.dspark_write_ctx_kv(b, st["ctx_hidden"], st["positions"], st["cos_sin"], st["cache_loc"],
                            st["k_pools"], st["v_pools"])
+    # the asynchronous read (pinned host word, no synchronisation of its own)
+    # and the synchronous one agree
+    word = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    dk.dspark_read_device_status_async(b, word)
+    torch.cuda.synchronize()
+    assert int(word[0]) == (dk.FLAG_POS_RANGE | dk.FLAG_LOC_RANGE)
     flags = dk.dspark_get_device_status(b)
     assert flags == (dk.FLAG_POS_RANGE | dk.FLAG_LOC_RANGE)
     expect = np.sort(np.delete(w.cache_loc, [3, 5, 7]))
