@@ -349,6 +349,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
   const int n_chunks = ctx_chunks + (has_ext ? 1 : 0);
   const int nwg = p.rows / kWgRows;              // softmax warpgroups with rows (2 or 4)
 
+  // The first slot-index loads and the Q copies are issued before the set-up
+  // barrier (Q's arrival on q_full follows it), so that their latency overlaps
+  // the barrier initialisation and the TMEM allocation.
+  const bool is_prod = warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps;
+  const int pw = warp - kProdWarp0;               // producer warp (producers only)
+  // producers: slot of key kKeysPerProdWarp*pw + lane of chunk c (checked
+  // where used), kNoKey past the context, or the row of the block's own key
+  auto lane_slot = [&](int c) -> int64_t {
+    const int key = kKeysPerProdWarp * pw + lane;
+    if (c >= n_chunks || lane >= kKeysPerProdWarp) return kNoKey;
+    if (c < ctx_chunks) {
+      const int64_t t = lo + static_cast<int64_t>(c) * kKeys + key;
+      return t < hi ? p.kv_indices[k0 + t] : kNoKey;
+    }
+    return key < p.block ? b * p.block + key : kNoKey;
+  };
+  // softmax: slot of this thread's key (warp % 4 * 32 + lane) in context chunk c
+  auto key_slot = [&](int c) -> int64_t {
+    if (c >= ctx_chunks) return 0;
+    const int64_t t = lo + static_cast<int64_t>(c) * kKeys + (warp % 4) * 32 + lane;
+    return t < hi ? p.kv_indices[k0 + t] : -1;
+  };
+  int64_t pre0 = 0, pre1 = 0;
+  if (is_prod) {
+    const int pt = threadIdx.x - kProdWarp0 * 32;
+    const E* q = static_cast<const E*>(p.q);
+    // Q of head g: row r = i*group + hh, its D columns as D/64 128-byte rows
+    for (int x = pt; x < p.rows * (D / 8); x += kProdThreads) {
+      const int r = x / (D / 8), u = x % (D / 8);
+      const E* src = q + ((b * p.block + r / p.group) * p.nq + g * p.group + r % p.group) * D + u * 8;
+      const uint32_t dst = smem_u32(smem + L.q_off) + (u / 8) * (kQRows * 128) + r * 128 + (((u % 8) ^ (r & 7)) * 16);
+      cp_async16(dst, src);
+    }
+    pre0 = lane_slot(0);
+    pre1 = lane_slot(1);
+  } else if (warp < kSoftWarps && warp / 4 < nwg) {
+    pre0 = key_slot(0);
+    pre1 = key_slot(1);
+  }
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAttnStages; ++i) {
       mbar_init(smem_u32(&bars->full_k[i]), kProdThreads);
@@ -376,23 +416,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
 
-  if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdThreads / 32) {
+  if (is_prod) {
     // ------------------------------------------------------------ producers
     // Every copy is a 16-byte asynchronous copy; the mbarrier of a half stage
     // (K or V rows of a chunk) completes when all 128 producer threads' copies
     // issued before their arrival on it have landed, so nothing here waits
     // for its own copies and up to three chunks are in flight.
     const int pt = threadIdx.x - kProdWarp0 * 32;   // 0..127 among the producers
-    const int pw = pt / 32;                         // producer warp
-    const E* q = static_cast<const E*>(p.q);
-    // Q of head g: row r = i*group + hh, its D columns as D/64 128-byte rows
-    for (int x = pt; x < p.rows * (D / 8); x += kProdThreads) {
-      const int r = x / (D / 8), u = x % (D / 8);
-      const E* src = q + ((b * p.block + r / p.group) * p.nq + g * p.group + r % p.group) * D + u * 8;
-      const uint32_t dst = smem_u32(smem + L.q_off) + (u / 8) * (kQRows * 128) + r * 128 + (((u % 8) ^ (r & 7)) * 16);
-      cp_async16(dst, src);
-    }
-    cp_async_arrive_noinc(smem_u32(&bars->q_full));
+    cp_async_arrive_noinc(smem_u32(&bars->q_full));   // the Q copies issued above
     // Warp pw copies kKeysPerProdWarp keys of a chunk; lane l learns the
     // slot of its key l two chunks ahead (the index load's latency under
     // the gather's DRAM load exceeds a chunk).  A warp instruction covers whole
@@ -402,18 +433,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
     constexpr int kPerIter = 32 / kUnits;         // keys per warp instruction
     constexpr int kXs = 8 / kPerIter;             // distinct swizzle rows of a lane's copies
     const int sub = lane / kUnits, u = lane % kUnits;
-    // slot of key kKeysPerProdWarp*pw + lane of chunk c (issued here, checked
-    // where used), kNoKey past the context, or the row of the block's own key
-    auto lane_slot = [&](int c) -> int64_t {
-      const int key = kKeysPerProdWarp * pw + lane;
-      if (c >= n_chunks || lane >= kKeysPerProdWarp) return kNoKey;
-      if (c < ctx_chunks) {
-        const int64_t t = lo + static_cast<int64_t>(c) * kKeys + key;
-        return t < hi ? p.kv_indices[k0 + t] : kNoKey;
-      }
-      return key < p.block ? b * p.block + key : kNoKey;
-    };
-    int64_t slot_cur = lane_slot(0), slot_nxt = lane_slot(1);
+    int64_t slot_cur = pre0, slot_nxt = pre1;
     bool ok_run = true;
     for (int c = 0; c < n_chunks && ok_run; ++c) {
       const int st = c % kAttnStages;
@@ -563,12 +583,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
     float m_run = -INFINITY, l_run = 0.f;
     uint8_t* p_smem = smem + L.p_off;
     bool done_ok = true;
-    auto key_slot = [&](int c) -> int64_t {   // slot of this thread's key in context chunk c
-      if (c >= ctx_chunks) return 0;
-      const int64_t t = lo + static_cast<int64_t>(c) * kKeys + k;
-      return t < hi ? p.kv_indices[k0 + t] : -1;
-    };
-    int64_t slot_cur = key_slot(0), slot_nxt = key_slot(1);   // loaded two chunks early
+    int64_t slot_cur = pre0, slot_nxt = pre1;   // loaded two chunks early
     for (int c = 0; c < n_chunks; ++c) {
       const int par = c & 1;
       bool valid;
