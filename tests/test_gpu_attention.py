@@ -69,6 +69,32 @@ def test_matches_oracle(batch, block, nq, nkv, D, lo, hi, dtype):
     check(a, out)
 
 
+def _widen_bf16(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+@pytest.mark.parametrize("lo,hi", [(600, 900), (2500, 3000)], ids=["one-split", "splits"])
+def test_growing_scores_force_rescales(lo, hi):
+    """Keys whose magnitude grows from chunk to chunk (x(1 + 4c) for the keys
+    of the c-th 128-key chunk of every context, x40 for the block's own keys):
+    every 32-key group's running maximum then grows by more than 2^8 in most
+    chunks, so the lazy rescale of O^T (by all warps of a warpgroup, for the
+    groups whose maximum grew) runs in every chunk, within a split, across
+    context splits and in the chunk of the block's own keys."""
+    import dataclasses
+    a = synthetic.make_attention_workload(3 if hi < 2048 else 2, 8, 32, 8, 128, lo, hi)
+    kp = _widen_bf16(a.k_pool)
+    for b in range(a.batch):
+        s0, s1 = int(a.kv_start[b]), int(a.kv_start[b + 1])
+        grow = 1.0 + 4.0 * (np.arange(s1 - s0) // 128)
+        kp[a.kv_indices[s0:s1]] *= grow[:, None, None].astype(np.float32)
+    a = dataclasses.replace(a, k_pool=synthetic.to_bits(kp, "bf16"),
+                            k_ext=synthetic.to_bits(_widen_bf16(a.k_ext) * np.float32(40.0), "bf16"))
+    out, status = run(a)
+    assert status == 0
+    check(a, out)
+
+
 def test_bench_launch_configuration_sampled():
     """The bench's launch configuration (64 requests of 8 x 32 heads over 8 KV
     heads of 128, bf16, contexts up to 32768: the same context split and
