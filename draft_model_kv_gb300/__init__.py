@@ -24,6 +24,7 @@ __all__ = [
     "dspark_status_string", "dspark_set_trace_buffer", "dspark_write_ctx_kv_noalloc", "dspark_set_split_wait_test",
     "dspark_set_kernel_variant", "dspark_describe_schedule", "dspark_bind_pools", "PoolSet", "dspark_qk_norm_rope",
     "dspark_correct_drafts_and_bonus", "dspark_draft_attention", "dspark_draft_attention_workspace_bytes",
+    "dspark_draft_attention_set_wait_test",
     "Combine", "dspark_pack_combine", "dspark_combine_hidden_states", "dspark_combine_get_status",
     "Fused", "dspark_pack_fused_ctx_kv", "dspark_combine_write_ctx_kv", "dspark_fused_get_status",
     "dspark_fused_clear_status",
@@ -435,6 +436,13 @@ def dspark_draft_attention(q, k_ext, v_ext, k_pool, v_pool, kv_indices, kv_start
         _stream_handle(stream))
     _abi.check(code, "dspark_draft_attention")
     return out
+
+
+def dspark_draft_attention_set_wait_test(limit_ns: int) -> None:
+    """Diagnostics: with limit_ns > 0, later dspark_draft_attention calls take
+    their timeout path after a wait of limit_ns (DSPARK_FLAG_TIMEOUT in the
+    status word, output incomplete); 0 switches it off."""
+    _abi.check(load().dspark_draft_attention_set_wait_test(int(limit_ns)), "dspark_draft_attention_set_wait_test")
 
 
 class Combine:

@@ -130,6 +130,8 @@ def load() -> ctypes.CDLL:
     lib.dspark_draft_attention.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp, vp, i64, i32, i32, i32, i32, i32,
                                            ctypes.c_float, i64, vp, vp, i64, vp, vp]
     lib.dspark_draft_attention.restype = ctypes.c_int
+    lib.dspark_draft_attention_set_wait_test.argtypes = [ctypes.c_uint64]
+    lib.dspark_draft_attention_set_wait_test.restype = ctypes.c_int
     lib.dspark_pack_combine.argtypes = [vp, i64, i64, i64, i32, vp, i32, ctypes.c_float, vp, ctypes.POINTER(vp)]
     lib.dspark_pack_combine.restype = ctypes.c_int
     lib.dspark_combine_hidden_states.argtypes = [vp, vp, i64, i64, vp, i64, vp]

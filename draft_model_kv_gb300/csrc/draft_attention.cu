@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -118,6 +119,7 @@ struct AttnParams {
   float* ws_o;      // [batch][splits][nkv*rows][D]
   float* ws_ml;     // [batch][splits][nkv*rows][2]
   uint32_t* status;
+  uint64_t test_wait_ns;   // diagnostics: 0, or the bound of a wait that never completes
 };
 
 template <typename E>
@@ -172,6 +174,7 @@ struct AttnBarriers {
   uint64_t pv_done[2];   // the O product of chunk c, per P buffer c & 1
   uint64_t q_full;
   uint64_t drain;
+  uint64_t never;                   // diagnostics: a barrier nothing arrives on
   uint32_t tmem_base;
   int abort;
 };
@@ -404,6 +407,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
     }
     mbar_init(smem_u32(&bars->q_full), kProdThreads);
     mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->never), 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -499,6 +503,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
       const uint32_t q_addr = smem_u32(smem + L.q_off);
       const uint32_t p_addr = smem_u32(smem + L.p_off);
       bool ok = attn_wait(smem_u32(&bars->q_full), 0, abort_flag, kAttnWaitNs);
+      // diagnostics (dspark_draft_attention_set_wait_test): a wait that runs
+      // out, so that every role takes its timeout path
+      if (ok && p.test_wait_ns != 0) ok = attn_wait(smem_u32(&bars->never), 0, abort_flag, p.test_wait_ns);
       fence_proxy_async_smem();   // the copies landed through the generic proxy; the MMAs read via the async one
       bool issued = false;
       int next_s = 0, next_pv = 0;
@@ -794,6 +801,8 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+std::atomic<uint64_t> g_attn_test_wait_ns{0};   // dspark_draft_attention_set_wait_test
+
 int sm103_attn(int device) {
   static int cache[64] = {0};
   const int d = device & 63;
@@ -891,6 +900,7 @@ extern "C" int dspark_draft_attention(const void* q, const void* k_ext, const vo
   p.ws_o = static_cast<float*>(workspace);
   p.ws_ml = p.ws_o + rows_all * pl.splits * head_dim;
   p.status = status;
+  p.test_wait_ns = g_attn_test_wait_ns.load();
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   cudaError_t e;
   if (dtype == DSPARK_DTYPE_BF16)
@@ -899,4 +909,9 @@ extern "C" int dspark_draft_attention(const void* q, const void* k_ext, const vo
   else
     e = head_dim == 128 ? launch_attention<__half, 128>(p, stream) : launch_attention<__half, 64>(p, stream);
   return e == cudaSuccess ? DSPARK_OK : DSPARK_E_CUDA;
+}
+
+extern "C" int dspark_draft_attention_set_wait_test(uint64_t limit_ns) {
+  dspark::g_attn_test_wait_ns.store(limit_ns);
+  return DSPARK_OK;
 }

@@ -83,6 +83,18 @@ DSPARK_API int dspark_draft_attention(const void* q, const void* k_ext, const vo
                                       void* workspace, int64_t workspace_bytes, uint32_t* status_flags,
                                       void* stream);
 
+/*
+ * dspark_draft_attention_set_wait_test -- diagnostics: with limit_ns > 0,
+ * every later dspark_draft_attention call in this process makes its split
+ * kernel's MMA issuer wait (bounded by limit_ns) on a barrier that nothing
+ * arrives on, so that every role of the kernel takes its timeout path: the
+ * call returns, DSPARK_FLAG_TIMEOUT is OR-ed into status_flags and the output
+ * is incomplete.  0 switches it off (the default).  Not for production use;
+ * process-wide, not synchronised with calls in flight on other threads.
+ * Returns DSPARK_OK.
+ */
+DSPARK_API int dspark_draft_attention_set_wait_test(uint64_t limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

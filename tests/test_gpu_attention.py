@@ -95,6 +95,23 @@ def test_growing_scores_force_rescales(lo, hi):
     check(a, out)
 
 
+def test_timeout_branch_returns_flags_and_leaves_the_context_usable():
+    """A split-kernel wait that nothing completes (diagnostics switch, 20 us
+    bound): the call returns with DSPARK_FLAG_TIMEOUT (0x4) in the status word;
+    afterwards, switched off, the same inputs give the oracle's output."""
+    import draft_model_kv_gb300 as dk
+    a = synthetic.make_attention_workload(3, 8, 32, 8, 128, 300, 700)
+    dk.dspark_draft_attention_set_wait_test(20_000)
+    try:
+        _, status = run(a)
+    finally:
+        dk.dspark_draft_attention_set_wait_test(0)
+    assert status & 0x4
+    out, status = run(a)
+    assert status == 0
+    check(a, out)
+
+
 def test_bench_launch_configuration_sampled():
     """The bench's launch configuration (64 requests of 8 x 32 heads over 8 KV
     heads of 128, bf16, contexts up to 32768: the same context split and
