@@ -591,6 +591,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
     uint8_t* p_smem = smem + L.p_off;
     bool done_ok = true;
     int64_t slot_cur = pre0, slot_nxt = pre1;   // loaded two chunks early
+    // byte offset in a P buffer of P^T[row wg*R + r][key k]: row Rw of block
+    // k/64, 16-byte unit (k%64)/8 XOR-swizzled by the row
+    uint32_t p_row[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int Rw = wg * R + r;
+      p_row[r] = static_cast<uint32_t>((k / 64) * (kQRows * 128) + (k % 8) * 2 + Rw * 128 +
+                                       ((((k % 64) / 8) ^ (Rw & 7)) * 16));
+    }
     for (int c = 0; c < n_chunks; ++c) {
       const int par = c & 1;
       bool valid;
@@ -631,21 +640,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const float mr = __shfl_sync(0xffffffffu, m_run, r);
-          pr[r] = (x[r] == -INFINITY || mr == -INFINITY) ? 0.f : fast_exp2(fmaf(x[r], p.scale_log2, -mr));
+          // a masked key (x = -inf) gives 2^-inf = 0; a row without a valid key
+          // so far in this warp (mr = -inf) has only masked keys
+          pr[r] = mr == -INFINITY ? 0.f : fast_exp2(fmaf(x[r], p.scale_log2, -mr));
         }
         // P buffer par was read by the product of chunk c - 2
         ok = c < 2 || __all_sync(0xffffffffu, attn_wait(smem_u32(&bars->pv_done[par]),
                                                         static_cast<uint32_t>((c >> 1) - 1) & 1u, abort_flag,
                                                         kAttnWaitNs));
         if (ok) {
-          // P^T[row][key] in the model dtype: row Rw of block k/64, 16-byte
-          // unit (k%64)/8 XOR-swizzled by the row
-          uint8_t* pb = p_smem + par * (2 * kQRows * 128) + (k / 64) * (kQRows * 128) + (k % 8) * 2;
+          // P^T[row][key] in the model dtype (the row offsets of this thread's
+          // key are fixed: p_row[r] below)
+          uint8_t* pb = p_smem + par * (2 * kQRows * 128);
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const int Rw = wg * R + r;
-            *reinterpret_cast<uint16_t*>(pb + Rw * 128 + ((((k % 64) / 8) ^ (Rw & 7)) * 16)) = to_bits<E>(pr[r]);
-          }
+          for (int r = 0; r < R; ++r) *reinterpret_cast<uint16_t*>(pb + p_row[r]) = to_bits<E>(pr[r]);
         }
         const float sum = warp_rows<false, R>(pr, lane);
         l_run = l_run * al + sum;
