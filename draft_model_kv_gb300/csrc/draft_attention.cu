@@ -465,8 +465,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint64_t* empty = half == 0 ? &bars->empty_k[st] : &bars->empty_v[st];
+        // warp-uniform outcome: the copy loop below shuffles across the warp
         if (c >= kAttnStages &&
-            !attn_wait(smem_u32(empty), static_cast<uint32_t>(c / kAttnStages - 1) & 1u, abort_flag, kAttnWaitNs)) {
+            !__all_sync(0xffffffffu, attn_wait(smem_u32(empty), static_cast<uint32_t>(c / kAttnStages - 1) & 1u,
+                                               abort_flag, kAttnWaitNs))) {
           ok_run = false;
           break;
         }
