@@ -757,40 +757,81 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
 }
 
 // Stage 2: one warp per (request, query row of a KV head): merge the splits.
+// Lane j holds split 32i + j's maximum and sum; each lane owns D/32
+// consecutive columns of the row.  The first kAhead splits' partial O and the
+// lanes' maxima and sums are loaded before the request's split count is known
+// (the workspace holds p.splits splits, written or not; the unwritten ones are
+// never used), so that a two-split row costs one round trip to memory.
 template <typename E, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const AttnParams p) {
+  constexpr int kPer = D / 32;   // 4 (D = 128) or 2 (D = 64) consecutive columns per lane
+  constexpr int kAhead = 4;      // splits of partial O in flight at once
+  using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
   const int nrows = p.nkv * p.rows;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kCombineWarps + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (wid >= p.batch * nrows) return;
   const int64_t b = wid / nrows;
   const int row = static_cast<int>(wid % nrows);
+  const int64_t r0 = b * p.splits * static_cast<int64_t>(nrows) + row;
+  const float2* ml_row = reinterpret_cast<const float2*>(p.ws_ml) + r0;
+  const float* src = p.ws_o + r0 * D + lane * kPer;
+  const int64_t s_stride = static_cast<int64_t>(nrows) * D;
+  Vec v[kAhead];
+#pragma unroll
+  for (int j = 0; j < kAhead; ++j)
+    if (j < p.splits) v[j] = *reinterpret_cast<const Vec*>(src + j * s_stride);
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < p.splits) ml = ml_row[static_cast<int64_t>(lane) * nrows];
   int64_t n_b = p.kv_start[b + 1] - p.kv_start[b];
   if (n_b > p.max_context) n_b = p.max_context;
   if (n_b < 0 || p.pool_slots <= 0) n_b = 0;
   int n_split = static_cast<int>((n_b + p.split_tokens - 1) / p.split_tokens);
   if (n_split < 1) n_split = 1;
-  const int64_t r0 = b * p.splits * static_cast<int64_t>(nrows) + row;
-  float M = -INFINITY;
-  for (int s = 0; s < n_split; ++s) M = fmaxf(M, p.ws_ml[(r0 + static_cast<int64_t>(s) * nrows) * 2]);
-  constexpr int kPer = D / 32;
-  float o[kPer] = {};
-  float Lsum = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    const int64_t r = r0 + static_cast<int64_t>(s) * nrows;
-    const float m = p.ws_ml[r * 2], l = p.ws_ml[r * 2 + 1];
-    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-    Lsum += w * l;
-    const float* src = p.ws_o + r * D + lane * kPer;
+  if (lane >= n_split) ml = make_float2(-INFINITY, 0.f);
+  float M = ml.x;
+  for (int s = lane + 32; s < n_split; s += 32) M = fmaxf(M, ml_row[static_cast<int64_t>(s) * nrows].x);
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) o[k] += w * src[k];
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float o_acc[kPer] = {};
+  float Lsum = 0.f;
+  for (int s0 = 0; s0 < n_split; s0 += 32) {
+    const int cnt = n_split - s0 < 32 ? n_split - s0 : 32;
+    if (s0 > 0) ml = lane < cnt ? ml_row[static_cast<int64_t>(s0 + lane) * nrows] : make_float2(-INFINITY, 0.f);
+    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+    Lsum += w * ml.y;
+    for (int j0 = 0; j0 < cnt; j0 += kAhead) {
+      if (s0 > 0 || j0 > 0) {
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j)
+          if (j0 + j < cnt) v[j] = *reinterpret_cast<const Vec*>(src + (s0 + j0 + j) * s_stride);
+      }
+#pragma unroll
+      for (int j = 0; j < kAhead; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+        if (j0 + j < cnt) {
+          const float* x = reinterpret_cast<const float*>(&v[j]);
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) o_acc[k] += wj * x[k];
+        }
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
   const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
   const int g = row / p.rows, rr = row % p.rows;
   const int i = rr / p.group, hh = rr % p.group;
   uint16_t* dst = static_cast<uint16_t*>(p.out) + ((b * p.block + i) * p.nq + g * p.group + hh) * D + lane * kPer;
+  uint32_t packed[kPer / 2];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) dst[k] = to_bits<E>(o[k] * inv);
+  for (int k = 0; k < kPer / 2; ++k)
+    packed[k] = static_cast<uint32_t>(to_bits<E>(o_acc[2 * k] * inv)) |
+                (static_cast<uint32_t>(to_bits<E>(o_acc[2 * k + 1] * inv)) << 16);
+  if constexpr (kPer == 4)
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+  else
+    *reinterpret_cast<uint32_t*>(dst) = packed[0];
 }
 
 template <typename E, int D>

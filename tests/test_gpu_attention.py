@@ -61,7 +61,8 @@ def check(a, out, requests=None, kv_start=None, kv_indices=None):
     (5, 16, 16, 8, 128, 0, 40, "bf16"),       # block 16, group 2, empty contexts
     (6, 4, 16, 4, 128, 17, 90, "bf16"),       # 16 rows per KV head (8 warps)
     (3, 8, 32, 8, 128, 50, 400, "fp16"),
-], ids=["decode", "d64", "long", "block16", "rows16", "fp16"])
+    (1, 8, 32, 8, 128, 29000, 30000, "bf16"),  # one request: more than 32 splits to merge
+], ids=["decode", "d64", "long", "block16", "rows16", "fp16", "splits34"])
 def test_matches_oracle(batch, block, nq, nkv, D, lo, hi, dtype):
     a = synthetic.make_attention_workload(batch, block, nq, nkv, D, lo, hi, dtype=dtype)
     out, status = run(a)
