@@ -328,6 +328,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const AttnPara
   constexpr int kBlocksD = D / 64;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // the merge kernel (a programmatic dependent launch) may be scheduled once
+  // every CTA of this grid has started; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the KV heads of one (request, split) are adjacent CTAs
   const int64_t b = blockIdx.z;
   const int g = blockIdx.x;
@@ -777,13 +780,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const 
   const float2* ml_row = reinterpret_cast<const float2*>(p.ws_ml) + r0;
   const float* src = p.ws_o + r0 * D + lane * kPer;
   const int64_t s_stride = static_cast<int64_t>(nrows) * D;
+  const int64_t kv0 = p.kv_start[b], kv1 = p.kv_start[b + 1];
+  // the split kernel's workspace writes are complete and visible past here
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   Vec v[kAhead];
 #pragma unroll
   for (int j = 0; j < kAhead; ++j)
     if (j < p.splits) v[j] = *reinterpret_cast<const Vec*>(src + j * s_stride);
   float2 ml = make_float2(-INFINITY, 0.f);
   if (lane < p.splits) ml = ml_row[static_cast<int64_t>(lane) * nrows];
-  int64_t n_b = p.kv_start[b + 1] - p.kv_start[b];
+  int64_t n_b = kv1 - kv0;
   if (n_b > p.max_context) n_b = p.max_context;
   if (n_b < 0 || p.pool_slots <= 0) n_b = 0;
   int n_split = static_cast<int>((n_b + p.split_tokens - 1) / p.split_tokens);
@@ -844,10 +850,21 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
   k1<<<grid, kAttnThreads, L.total, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // the merge is a programmatic dependent launch: its CTAs may take the SMs
+  // that the split kernel's last CTAs leave idle, and wait there for it
   const int64_t rows = p.batch * p.nkv * p.rows;
-  attn_combine_kernel<E, D><<<static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps),
-                              kCombineWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps));
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel<E, D>, p);
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
