@@ -12,7 +12,8 @@ requests x 8-token windows) and `--tokens T` give the other lines.
 
 Prints ONE JSON line (rank 0).  `value` is device time: CUDA events on the
 launching stream around each step, inputs resident in HBM, the L2 flushed
-(256 MiB write) between steps outside the events, and the step enqueued
+between steps outside the events (a 256 MiB write, then a 256 MiB read that
+writes the flush's dirty lines back before the step), and the step enqueued
 before its start event fires (a short device-side delay precedes it).  `e2e` is the same metric
 through the public API with pinned host inputs: host->device copies of the
 step's inputs, the write, and a device->host read of the status word, timed
@@ -40,6 +41,27 @@ METRIC = "ctx-KV tokens/s (stacked proj+norm+RoPE+pool write); % of roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 SLEEP_CYCLES = 200_000          # ~0.1 ms of GPU time between the L2 flush and a timed step
+L2_NOTE = "flushed between steps (256 MiB write, then a 256 MiB read that writes the dirty lines back)"
+
+
+class L2Flush:
+    """Empties L2 of a step's inputs between timed steps: a write of
+    L2_FLUSH_BYTES, then a read of another L2_FLUSH_BYTES buffer.  The write
+    alone would leave L2 full of dirty lines, and the next step would pay for
+    writing them back to DRAM (about 129 MB, up to 8 us of a DRAM-bound
+    kernel); the read makes those write-backs happen before the step, and L2
+    then holds clean lines of a buffer the step never touches."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=device)
+        self.out = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self, v):
+        import torch
+        self.w.fill_(v)
+        torch.sum(self.r, out=self.out)
 
 
 def peaks():
@@ -220,7 +242,7 @@ def config_of(w, flush=True):
     import synthetic
     c = synthetic.describe(w)
     c["parallelism"] = "replicas (one independent write per GPU, no collective)"
-    c["l2"] = "flushed between steps (256 MiB write)" if flush else "n/a (CPU)"
+    c["l2"] = L2_NOTE if flush else "n/a (CPU)"
     return c
 
 
@@ -241,7 +263,7 @@ def run_gpu(args, w):
         lay.qkv_weight = None
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
+    flush = L2Flush(f"cuda:{local}")
     n_written = written_rows(w)
     pools = dk.dspark_bind_pools(bundle, st["k_pools"], st["v_pools"])
 
@@ -253,7 +275,7 @@ def run_gpu(args, w):
                                loc_row_width=st["loc_row_width"], stream=stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         step()
     dk.dspark_clear_device_status(bundle)
     torch.cuda.synchronize()
@@ -265,7 +287,7 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i & 0xFF)
             # a short device-side delay lets the host enqueue the step before its
             # start event fires, so the events bracket device work only
             torch.cuda._sleep(SLEEP_CYCLES)
@@ -307,7 +329,7 @@ def run_gpu(args, w):
     e2e_total = 0.0
     e2e_steps = max(1, min(args.steps, 200))
     for i in range(e2e_steps + 3):
-        flush.fill_(i & 0xFF)
+        flush(i & 0xFF)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         dev_buf.copy_(host_buf, non_blocking=True)
@@ -486,14 +508,14 @@ def run_qk(args):
     cs = torch.from_numpy(q.cos_sin).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def step(xx=x, pp=pos):
         dk.dspark_qk_norm_rope(xx, pp, qw, kwt, cs, q.num_q_heads, q.num_k_heads, q.D, q.eps,
                                status_flags=status, stream=stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -501,7 +523,7 @@ def run_qk(args):
     barrier()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i & 0xFF)
             torch.cuda._sleep(SLEEP_CYCLES)
             starts[i].record(stream)
             step()
@@ -522,7 +544,7 @@ def run_qk(args):
     host_pos = pos.cpu().pin_memory()
     e2e_total, e2e_steps = 0.0, max(1, min(args.steps, 100))
     for i in range(e2e_steps + 3):
-        flush.fill_(i & 0xFF)
+        flush(i & 0xFF)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         x.copy_(host_x, non_blocking=True)
@@ -544,7 +566,7 @@ def run_qk(args):
         "config": {"workload": f"qk_norm_rope/{q.name}", "tokens": q.T, "num_q_heads": q.num_q_heads,
                    "num_k_heads": q.num_k_heads, "head_dim": q.D, "dtype": q.dtype,
                    "parallelism": "replicas (one independent pass per GPU, no collective)",
-                   "l2": "flushed between steps (256 MiB write)"},
+                   "l2": L2_NOTE},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                      "traffic_source": traffic_note, "peak_source": pk["source"]},
@@ -593,9 +615,9 @@ def run_verify(args):
     dev = f"cuda:{local}"
     dc, dt_ = torch.from_numpy(cand).to(dev), torch.from_numpy(tgt).to(dev)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         dk.dspark_correct_drafts_and_bonus(dc, dt_, stream=stream)
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -603,7 +625,7 @@ def run_verify(args):
     barrier()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i & 0xFF)
             torch.cuda._sleep(SLEEP_CYCLES)
             starts[i].record(stream)
             dk.dspark_correct_drafts_and_bonus(dc, dt_, stream=stream)
@@ -637,7 +659,7 @@ def run_verify(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": {"workload": f"verify/{w.name}", "batch": batch, "block": block,
                    "parallelism": "replicas (one independent step per GPU, no collective)",
-                   "l2": "flushed between steps (256 MiB write)"},
+                   "l2": L2_NOTE},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
                      "note": "launch-bound: a few KB per launch"},
@@ -699,14 +721,14 @@ def run_attention(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     scale = D ** -0.5
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def step():
         dk.dspark_draft_attention(q, ke, ve, kp, vp, idx, start, scale, max_ctx, out=out, workspace=work,
                                   status_flags=status, stream=stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -714,7 +736,7 @@ def run_attention(args):
     barrier()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i & 0xFF)
             torch.cuda._sleep(SLEEP_CYCLES)
             starts[i].record(stream)
             step()
@@ -757,7 +779,7 @@ def run_attention(args):
         "config": {"workload": "draft_attention/decode512", "requests": batch, "block": block,
                    "num_q_heads": nq, "num_kv_heads": nkv, "head_dim": D, "context_tokens": ctx_total,
                    "max_context": max_ctx, "parallelism": "replicas (one independent pass per GPU, no collective)",
-                   "l2": "flushed between steps (256 MiB write); inputs larger than L2"},
+                   "l2": L2_NOTE + "; inputs larger than L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                      "traffic_source": traffic_note, "peak_source": pk["source"]},
@@ -819,7 +841,7 @@ def run_fused(args):
     torch.cuda.empty_cache()
     aux = bits_to_tensor(cw.aux, dt, dev)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     n_written = written_rows(w)
 
     def step(a=None, pos=None, loc=None, cl=None):
@@ -829,7 +851,7 @@ def run_fused(args):
                                        loc_row_width=st["loc_row_width"], stream=stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         step()
     dk.dspark_fused_clear_status(f)
     torch.cuda.synchronize()
@@ -838,7 +860,7 @@ def run_fused(args):
     barrier()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i & 0xFF)
             torch.cuda._sleep(SLEEP_CYCLES)
             starts[i].record(stream)
             step()
@@ -872,7 +894,7 @@ def run_fused(args):
     h2d = sum(t.numel() * t.element_size() for t in parts)
     e2e_total, e2e_steps = 0.0, max(1, min(args.steps, 200))
     for i in range(e2e_steps + 3):
-        flush.fill_(i & 0xFF)
+        flush(i & 0xFF)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         dev_buf.copy_(host_buf, non_blocking=True)
@@ -959,13 +981,13 @@ def run_combine(args):
     aux = bits_to_tensor(cw.aux, dt, dev)
     out = torch.empty((cw.T, cw.hidden), dtype=dt, device=dev)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def step():
         dk.dspark_combine_hidden_states(c, aux, out=out, stream=stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -973,7 +995,7 @@ def run_combine(args):
     barrier()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i & 0xFF)
             torch.cuda._sleep(SLEEP_CYCLES)
             starts[i].record(stream)
             step()
@@ -993,7 +1015,7 @@ def run_combine(args):
     hout = torch.empty(out.shape, dtype=dt).pin_memory()
     e2e_total, e2e_steps = 0.0, max(1, min(args.steps, 100))
     for i in range(e2e_steps + 3):
-        flush.fill_(i & 0xFF)
+        flush(i & 0xFF)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         aux.copy_(hx, non_blocking=True)
@@ -1022,7 +1044,7 @@ def run_combine(args):
         "scaling": "weak", "vs_baseline": None, "dtype": cw.dtype, "data": "synthetic",
         "config": {"workload": f"combine/{args.workload}", "tokens": cw.T, "hidden": cw.hidden, "aux_dim": K,
                    "parallelism": "replicas (one independent pass per GPU, no collective)",
-                   "l2": "flushed between steps (256 MiB write)"},
+                   "l2": L2_NOTE},
         "roofline": primary, "roofline_other": other, "roofline_time_frac": max(t_tc, t_hbm) / t_step,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cw.T * K * 2,
                 "d2h_bytes_per_step": cw.T * cw.hidden * 2, "steps": e2e_steps},
@@ -1065,7 +1087,7 @@ def run_trace(args, w):
     bundle = dk.dspark_pack_ctx_kv(st["layers"], w.H)
     dk.dspark_set_kernel_variant(bundle, args.variant)
     pools = dk.dspark_bind_pools(bundle, st["k_pools"], st["v_pools"])
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush("cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     words = 64
     buf = torch.zeros(sms * words, dtype=torch.int64, device="cuda")
@@ -1075,13 +1097,13 @@ def run_trace(args, w):
                                commit_lens=st["commit_lens"], loc_row_width=st["loc_row_width"])
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         step()
     dk.dspark_set_trace_buffer(bundle, buf)
     lines = []
     for k in range(args.steps):
         buf.zero_()
-        flush.fill_(2)
+        flush(2)
         torch.cuda.synchronize()
         step()
         torch.cuda.synchronize()
