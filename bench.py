@@ -61,7 +61,7 @@ class L2Flush:
     def __call__(self, v):
         import torch
         self.w.fill_(v)
-        torch.sum(self.r, out=self.out)
+        torch.sum(self.r, dim=0, out=self.out)
 
 
 def peaks():
