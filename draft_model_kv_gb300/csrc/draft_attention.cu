@@ -32,6 +32,10 @@
 // oldest chunk whose P^T is written.  Each split writes its unnormalised O,
 // maximum and sum to the workspace; stage 2 merges the splits of each query
 // row with the log-sum-exp weights and stores the output in the model dtype.
+// Stage 2 is a programmatic dependent launch: its CTAs may start on SMs that
+// stage 1's last wave leaves idle and wait there (griddepcontrol.wait) for
+// stage 1 to complete.  Neither stage allocates or synchronises with the
+// host, so a call can be captured in a CUDA graph.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
