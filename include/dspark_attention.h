@@ -74,6 +74,13 @@ DSPARK_API int64_t dspark_draft_attention_workspace_bytes(int64_t batch, int32_t
  * unsupported head / block combination), DSPARK_E_DTYPE_MISMATCH,
  * DSPARK_E_POOL_LAYOUT, DSPARK_E_ALIGNMENT, DSPARK_E_SCRATCH_LIMIT
  * (workspace too small), DSPARK_E_DEVICE or DSPARK_E_CUDA.
+ *
+ * Enqueues two kernels on `stream`: the split kernel, then the merge as a
+ * programmatic dependent launch (its blocks may be scheduled while the split
+ * kernel's last blocks run, and read the workspace only once that kernel has
+ * completed).  No host synchronisation and no allocation: the call can be
+ * captured in a CUDA graph and replayed.  Calls that share a workspace must be
+ * ordered on the GPU.
  */
 DSPARK_API int dspark_draft_attention(const void* q, const void* k_ext, const void* v_ext, const void* k_pool,
                                       const void* v_pool, int64_t pool_row_stride, int64_t pool_slots,

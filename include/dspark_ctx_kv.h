@@ -165,7 +165,10 @@ DSPARK_API int dspark_pack_ctx_kv(const dspark_layer_desc* layers /* (host) [num
  * Written non-negative locs must be distinct.  A position outside the table or
  * a loc >= pool_slots is a caller error: that token is skipped and a device
  * status flag is set.  num_tokens == 0 returns DSPARK_OK at once.
- * Enqueues one kernel on `stream`; no host synchronisation.
+ * Enqueues one kernel on `stream`; no host synchronisation and no device
+ * allocation (the bundle's scratch is allocated by dspark_pack_ctx_kv), so the
+ * call can be captured in a CUDA graph and replayed; a replay reads the
+ * buffers' current contents.
  *
  * Concurrency.  Every write with a bundle uses that bundle's scratch: the
  * partial tiles of the work split, their arrival counters and the status

@@ -125,6 +125,19 @@ def test_bench_launch_configuration_sampled():
     check(a, out, requests=[0, 1, 63])
 
 
+@pytest.mark.parametrize("D,dtype", [(128, "fp16"), (64, "bf16")], ids=["fp16", "d64"])
+def test_full_size_launch_other_dtype_and_head_dim_sampled(D, dtype):
+    """The bench's launch shape (64 requests, 32 query / 8 KV heads, contexts
+    up to 32768: sixteen context splits) in fp16 and with head_dim 64: one
+    32768-token context, one of 20000 (a ragged last split) and 62 short ones;
+    those two and a short one are checked against the oracle."""
+    ctx = [32768, 20000] + [int(c) for c in np.random.default_rng(12).integers(1, 300, size=62)]
+    a = synthetic.make_attention_workload(64, 8, 32, 8, D, 0, 0, contexts=ctx, dtype=dtype)
+    out, flags = run(a, max_context=32768)
+    assert flags == 0
+    check(a, out, requests=[0, 1, 40])
+
+
 def test_bad_index_is_flagged_and_skipped():
     a = synthetic.make_attention_workload(3, 8, 32, 8, 128, 20, 60)
     idx = a.kv_indices.copy()
