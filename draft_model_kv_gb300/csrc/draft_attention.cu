@@ -64,7 +64,7 @@ constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kKeysPerProdWarp = kKeys / kProdWarps;
 constexpr int kAttnMmaWarp = kProdWarp0 + kProdWarps;   // the MMA issuer
 constexpr int kAttnThreads = (kAttnMmaWarp + 1) * 32;
-constexpr int kSplitGoal = 2048;         // context tokens per split aimed for
+constexpr int kSplitGoal = 8192;         // context tokens per split aimed for
 constexpr int kMaxSplitTokens = 8192;
 constexpr int kWaveCtas = 152;           // stage-1 CTAs resident at once (one per SM of a GB300)
 constexpr int kCombineWarps = 8;
@@ -84,14 +84,20 @@ struct AttnPlan {
 
 // Context split: about kSplitGoal tokens per split (a multiple of the chunk),
 // and more, shorter splits when batch x KV heads CTAs per split would not
-// fill two waves.  Depends on the sizes only, so the workspace size query and
-// the launch agree.
+// fill four waves.  Every CTA pays ~5 us of start and tail (the context
+// bounds, then the first chunk's slot indices, then its rows, before the
+// first product; the merge of its key groups and the workspace writes after
+// the last), so long splits pay off while enough CTAs remain to balance the
+// SMs: on 64 requests of 8 x 32 heads with contexts of 1k-32k tokens, splits
+// of 2048 / 4096 / 6144-12288 / 16384 tokens took 1015 / 937 / 922 / 947 us;
+// 4096-token contexts keep two splits of 2048.  Depends on the sizes only, so
+// the workspace size query and the launch agree.
 AttnPlan make_plan(int64_t batch, int nkv, int64_t max_context) {
   AttnPlan pl;
   if (batch < 1) batch = 1;
   int64_t splits = (max_context + kSplitGoal - 1) / kSplitGoal;
   const int64_t per_split = batch * nkv;
-  const int64_t want = (2 * kWaveCtas + per_split - 1) / per_split;
+  const int64_t want = (4 * kWaveCtas + per_split - 1) / per_split;
   if (splits < want) splits = want;
   if (splits < 1) splits = 1;
   int64_t c = (max_context + splits - 1) / splits;
