@@ -342,7 +342,7 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   p.num_m = static_cast<int32_t>((T + tile_rows - 1) / tile_rows);
   p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
   p.num_tiles = p.num_m * p.num_n;
-  const int workers = plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : singles, true, p);
+  const int workers = plan_schedule(p.num_tiles, p.num_kb, pair ? pairs : singles, true, p, true);
   give_leftover_to_v_tiles(p, workers);
   const int grid = pair ? 2 * workers : workers;
   const cudaError_t e =
@@ -406,7 +406,8 @@ int dspark_describe_schedule(int64_t tiles, int32_t num_kb, int32_t workers, int
   if (out == nullptr || tiles < 1 || tiles > 0x7FFFFFFF || num_kb < 1 || workers < 1) return DSPARK_E_INVALID_ARG;
   WriteParams p;
   std::memset(&p, 0, sizeof(p));
-  const int grid = plan_schedule(static_cast<int>(tiles), num_kb, workers, split_first_allowed != 0, p);
+  const int grid =
+      plan_schedule(static_cast<int>(tiles), num_kb, workers, split_first_allowed != 0, p, split_first_allowed != 0);
   out->workers = grid;
   out->whole_tiles = p.dp_tiles;
   out->split_units = p.sk_units;

@@ -124,11 +124,24 @@ inline size_t workspace_bytes(int ctas) {
 //    leftover tiles on 76 pairs, 4% with 24; slower from about 44 (a tile then
 //    has few contributors, each finishing many rows) and with two waves or
 //    more (the other order's split-tile costs are the smaller there).
+//  - fewer tiles than workers but at least half as many, with `whole_tiles`
+//    (the tiled write): each tile goes whole to one worker and the other
+//    workers stay idle.  Cut, every tile would be finished by adding a full
+//    fp32 partial tile that another worker published, which costs more than
+//    the idle workers' share of the products: at 256 tokens on 76 CTA pairs
+//    (40 tiles) the finishers spent ~6.5 us adding the other part.
 //  - otherwise: all but the last full wave run whole tiles and the rest (one
 //    to two waves' worth) is cut over all workers
-inline int plan_schedule(int tiles, int num_kb, int workers, bool split_first, WriteParams& p) {
+inline int plan_schedule(int tiles, int num_kb, int workers, bool split_first, WriteParams& p,
+                         bool whole_tiles = false) {
   const int waves = tiles / workers;
   p.sk_first = 0;
+  if (whole_tiles && tiles < workers && 2 * tiles >= workers) {
+    p.dp_tiles = tiles;
+    p.sk_units = 0;
+    p.sk_workers = 0;
+    return tiles;
+  }
   if (split_first && waves == 1 && 3 * (tiles - workers) <= workers) {
     p.sk_first = 1;
     p.dp_tiles = waves * workers;

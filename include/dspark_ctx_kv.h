@@ -326,7 +326,11 @@ typedef struct dspark_schedule_info {
  * each on up to `workers` workers (SMs for single-CTA tiles, SM pairs for CTA
  * pairs).  `split_first_allowed` is 1 for the tiled kernels and 0 for the
  * weight-streaming kernel.  Diagnostics: the kernels compute the same split
- * themselves.  One refinement is not shown: in the split-first order with
+ * themselves.  With `split_first_allowed` the split is the tiled write's,
+ * which gives every tile whole to one worker (and leaves the others idle)
+ * when there are fewer tiles than workers but at least half as many; the
+ * combine product and the allocation-free write cut those tiles instead.
+ * One refinement is not shown: in the split-first order with
  * one whole tile per worker, the write hands the leftover only to the
  * workers whose whole tile holds V heads (when each then takes 2 to 8
  * k-blocks), reordering the whole tiles so that those workers come first.

@@ -63,7 +63,7 @@ def check_against_oracle(w, kp, vp, sample=None):
 
 CASES = [
     ("stream", 16), ("stream", 64),   # weight streaming: every weight tile cut between ~2 SMs
-    ("single", 296),                  # 120 tiles on 152 SMs: all cut, finished by their last owner
+    ("single", 120),                  # 40 tiles on 152 SMs: all cut, finished by their last owner
     ("pair", 512),                    # 80 tiles on 76 pairs: split-first, leftover on the V-tile pairs
     ("pair", 1024),                   # 160 tiles: one wave of whole tiles, then 84 cut tiles
 ]
@@ -98,11 +98,14 @@ def test_split_wait_runs_out_and_bundle_recovers(variant, tokens):
     b.free()
 
 
-def test_split_wait_test_leaves_uncut_writes_alone():
-    """tiny: 2 tiles of 4 k-blocks go to one CTA whole, so no wait for other
-    CTAs exists and the diagnostic mode changes nothing."""
+@pytest.mark.parametrize("name,tokens", [("tiny", None), ("decode512", 296)], ids=["tiny", "single-296"])
+def test_split_wait_test_leaves_uncut_writes_alone(name, tokens):
+    """tiny: 2 tiles of 4 k-blocks go to one CTA whole; 296 tokens on single
+    CTAs: 120 tiles for 152 SMs, at least half as many tiles as workers, so
+    each goes whole to one CTA.  No wait for other CTAs exists and the
+    diagnostic mode changes nothing."""
     import draft_model_kv_gb300 as dk
-    w = synthetic.make_workload("tiny")
+    w = synthetic.make_workload(name, **({} if tokens is None else {"tokens": tokens}))
     st = stage(w)
     b = dk.dspark_pack_ctx_kv(st["layers"], w.H)
     dk.dspark_set_kernel_variant(b, "single")
