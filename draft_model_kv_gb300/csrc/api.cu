@@ -306,8 +306,17 @@ int dspark_write_ctx_kv(dspark_bundle_t b, const void* ctx_hidden, int64_t T,
   uint32_t stage_b = 0, acc_stride = 0, tmem_cols = 0;
   const bool stream_ok = b->KV % 128 == 0 &&
                          stream_plan(T, &t_pad, &stages, &stage_b, &acc_stride, &tmem_cols);
+  // AUTO: weight streaming up to kStreamAutoMaxTokens tokens, and up to
+  // kStreamAutoCutMaxTokens when the CTA pairs would have fewer than half as
+  // many tiles as pairs (every tile cut); above, the pairs take whole tiles
+  bool auto_stream = T <= kStreamAutoMaxTokens;
+  if (!auto_stream && T <= kStreamAutoCutMaxTokens) {
+    const int pairs_avail = pair_workers(device);
+    const int64_t pair_tiles = ((T + 2 * kTileM - 1) / (2 * kTileM)) * ((b->N + kTileN - 1) / kTileN);
+    auto_stream = pairs_avail <= 0 || 2 * pair_tiles < pairs_avail;
+  }
   const bool use_stream = stream_ok && (b->variant == DSPARK_VARIANT_STREAM ||
-                                        (b->variant == DSPARK_VARIANT_AUTO && T <= kStreamAutoMaxTokens));
+                                        (b->variant == DSPARK_VARIANT_AUTO && auto_stream));
   if (b->variant == DSPARK_VARIANT_STREAM && !stream_ok) return DSPARK_E_INVALID_ARG;
   if (use_stream) {
     CUtensorMap tmap_x;

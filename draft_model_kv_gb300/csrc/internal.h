@@ -103,7 +103,8 @@ constexpr int kTraceItems = (kTraceWords - 3) / 6;
 constexpr int kMinUnitsPerCta = 8;   // k-blocks: keeps small problems from over-splitting
 constexpr int kMinSplitUnits = 2;    // k-blocks per worker of the leftover tiles (split-first order)
 constexpr int kMaxLightShare = 8;    // k-blocks per V-tile worker when only those take the leftover
-constexpr int kStreamAutoMaxTokens = 128;   // AUTO picks the weight-streaming kernel up to here
+constexpr int kStreamAutoMaxTokens = 64;    // AUTO picks the weight-streaming kernel up to here,
+constexpr int kStreamAutoCutMaxTokens = 128; // and up to here when CTA pairs would cut every tile
 
 
 // Bytes of partial-tile workspace and arrival counters for a grid of `ctas`.

@@ -276,7 +276,9 @@ DSPARK_API int dspark_clear_device_status(dspark_bundle_t bundle, void* stream);
  *  STREAM: for num_tokens <= 256 (and num_kv_heads*head_dim a multiple of 128):
  *          128 weight rows x all tokens per tile, weights streamed by every SM;
  *          a write that does not meet those limits returns DSPARK_E_INVALID_ARG.
- *  AUTO (the default): STREAM when it applies and num_tokens <= 128, else PAIR.
+ *  AUTO (the default): STREAM when it applies and num_tokens <= 64, or
+ *        num_tokens <= 128 and the CTA pairs would get fewer tiles than half
+ *        their number (every tile cut); else PAIR.
  * Results agree within rounding; the choice only changes speed.  Returns
  * DSPARK_E_INVALID_ARG for other values. */
 #define DSPARK_VARIANT_AUTO 0

@@ -165,7 +165,7 @@ def test_many_contributors_per_split_tile(T, variant):
 @pytest.mark.parametrize("name,T", [("k3gqa", 64), ("fp16bias", 48), ("decode512", 200),
                                     ("decode512", 256)])
 def test_small_token_counts_other_shapes(name, T):
-    """The weight-streaming kernel (chosen automatically at T <= 128) on head
+    """The weight-streaming kernel (chosen automatically at T <= 64) on head
     dim 64, fp16 with bias, and token counts that are not a multiple of 32."""
     w = workload(name, tokens=T)
     st, _, flags = run_gpu(w, variant="stream")
