@@ -136,6 +136,28 @@ def test_decode_shapes_take_the_split_first_order():
     assert p["whole_tiles"] == 0 and p["workers"] == 1
 
 
+def test_whole_tiles_when_at_least_half_as_many_tiles_as_workers():
+    """The tiled write gives every tile whole to one worker (no cut tile, the
+    other workers idle) when there are fewer tiles than workers but at least
+    half as many; below half, and for the weight-streaming kernel
+    (split_first_allowed 0, which needs every SM streaming), the tiles are cut
+    over the workers as before."""
+    for workers in (64, 76, 152):
+        for tiles in range(1, workers):
+            p = dk.dspark_describe_schedule(tiles, 64, workers, True)
+            whole = 2 * tiles >= workers
+            if whole:
+                assert p == {"workers": tiles, "whole_tiles": tiles, "split_units": 0, "split_workers": 0,
+                             "split_first": 0}, (tiles, workers, p)
+            else:
+                assert p["whole_tiles"] == 0 and p["split_units"] == tiles * 64, (tiles, workers, p)
+            q = dk.dspark_describe_schedule(tiles, 64, workers, False)
+            assert q["whole_tiles"] == 0 and q["split_units"] == tiles * 64, (tiles, workers, q)
+    # 256 tokens on 76 CTA pairs: 40 tiles whole on 40 pairs; 20 (k3gqa) cut
+    assert dk.dspark_describe_schedule(40, 64, 76)["workers"] == 40
+    assert dk.dspark_describe_schedule(20, 112, 76)["whole_tiles"] == 0
+
+
 def test_refusals():
     with pytest.raises(dk.DSparkError):
         dk.dspark_describe_schedule(0, 64, 76)
