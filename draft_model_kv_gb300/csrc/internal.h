@@ -114,9 +114,14 @@ inline size_t workspace_bytes(int ctas) {
 
 // Work split of a problem of `tiles` output tiles with `num_kb` k-blocks
 // each on up to `workers` workers; sets p.dp_tiles, p.sk_units, p.sk_workers
-// and p.sk_first and returns the number of workers to launch.
-//  - fewer tiles than workers: every k-block is in the stream-K range, spread
-//    over at most one worker per kMinUnitsPerCta k-blocks
+// and p.sk_first and returns the number of workers to launch.  In the order
+// checked:
+//  - fewer tiles than workers but at least half as many, with `whole_tiles`
+//    (the tiled write): each tile goes whole to one worker and the other
+//    workers stay idle.  Cut, every tile would be finished by adding a full
+//    fp32 partial tile that another worker published, which costs more than
+//    the idle workers' share of the products: at 256 tokens on 76 CTA pairs
+//    (40 tiles) the finishers spent ~6.5 us adding the other part.
 //  - one full wave and at most a third of a wave left over, with
 //    `split_first` (kernels that implement it): the full wave runs whole tiles
 //    and the leftover tiles are cut over the workers, at least kMinSplitUnits
@@ -125,12 +130,9 @@ inline size_t workspace_bytes(int ctas) {
 //    leftover tiles on 76 pairs, 4% with 24; slower from about 44 (a tile then
 //    has few contributors, each finishing many rows) and with two waves or
 //    more (the other order's split-tile costs are the smaller there).
-//  - fewer tiles than workers but at least half as many, with `whole_tiles`
-//    (the tiled write): each tile goes whole to one worker and the other
-//    workers stay idle.  Cut, every tile would be finished by adding a full
-//    fp32 partial tile that another worker published, which costs more than
-//    the idle workers' share of the products: at 256 tokens on 76 CTA pairs
-//    (40 tiles) the finishers spent ~6.5 us adding the other part.
+//  - other problems with fewer tiles than workers: every k-block is in the
+//    stream-K range, spread over at most one worker per kMinUnitsPerCta
+//    k-blocks
 //  - otherwise: all but the last full wave run whole tiles and the rest (one
 //    to two waves' worth) is cut over all workers
 inline int plan_schedule(int tiles, int num_kb, int workers, bool split_first, WriteParams& p,
