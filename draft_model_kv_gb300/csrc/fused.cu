@@ -157,7 +157,9 @@ int dspark_combine_write_ctx_kv(dspark_fused_t f, const void* aux, int64_t T, in
   p.num_m = static_cast<int32_t>((T + 2 * kTileM - 1) / (2 * kTileM));
   p.num_n = static_cast<int32_t>((b->N + kTileN - 1) / kTileN);
   p.num_tiles = p.num_m * p.num_n;
-  p.workers = plan_schedule(p.num_tiles, p.num_kb, pairs, true, p);
+  // the write takes whole tiles when they number at least half the pairs, as
+  // the standalone write does
+  p.workers = plan_schedule(p.num_tiles, p.num_kb, pairs, true, p, true);
   give_leftover_to_v_tiles(p, p.workers);
   p.trace = nullptr;
   p.phase_count = f->phase_count;
